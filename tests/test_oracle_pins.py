@@ -1,0 +1,310 @@
+"""Pins for the oracle: checks against facts other than the oracle itself.
+
+Each pin is a closed form, an invariant the recurrence must satisfy, a brute
+force on tiny inputs, or an agreement between two independently written forms
+(sequential vs chunked).  Small odd dimensions (K != V) are used wherever a
+transposed operand or a row/column mix-up could otherwise hide.
+
+The pins are written as ``pin_*(orc)`` functions of an oracle namespace so that
+``test_pins_catch_planted_mistakes`` can run them against copies of the oracle
+source with a mistake planted in them.
+"""
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = []
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _unit_vecs(rng, n, d):
+    x = rng.standard_normal((n, d))
+    return x / np.linalg.norm(x, axis=1, keepdims=True)
+
+
+def _inputs(rng, T, K, V, gk_scale=1.0):
+    q = _unit_vecs(rng, T, K)
+    k = _unit_vecs(rng, T, K)
+    v = rng.standard_normal((T, V))
+    gk = -np.log1p(np.exp(gk_scale * rng.standard_normal((T, K))))   # -softplus
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(T)))               # sigmoid
+    return q, k, v, gk, beta
+
+
+# --------------------------------------------------------------------------
+# pins (each raises AssertionError when violated)
+# --------------------------------------------------------------------------
+
+def pin_single_token_closed_form(orc):
+    """S0 = 0, one token: S1 = beta k v^T and o1 = scale beta (k.q) v."""
+    rng = _rng(1)
+    K, V, scale = 5, 3, 0.7
+    q, k, v, gk, beta = _inputs(rng, 1, K, V)
+    o, S = orc.unit(q, k, v, gk, beta, np.zeros((K, V)), scale=scale)
+    np.testing.assert_allclose(S, beta[0] * np.outer(k[0], v[0]), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(o[0], scale * beta[0] * np.dot(k[0], q[0]) * v[0], rtol=1e-13,
+                               atol=1e-15)
+
+
+def pin_identity_when_no_write_no_decay(orc):
+    """beta = 0, gk = 0: the state is unchanged exactly and o_t = scale S0^T q_t."""
+    rng = _rng(2)
+    T, K, V, scale = 6, 5, 3, 1.3
+    q, k, v, _, _ = _inputs(rng, T, K, V)
+    S0 = rng.standard_normal((K, V))
+    o, S = orc.unit(q, k, v, np.zeros((T, K)), np.zeros(T), S0, scale=scale)
+    assert np.array_equal(S, S0)
+    np.testing.assert_allclose(o, scale * q @ S0, rtol=1e-13, atol=1e-14)
+
+
+def pin_pure_decay_closed_form(orc):
+    """beta = 0, gk_t = g for every t: S_T = Diag(exp(T g)) S0 (rows = key channels,
+    natural exponential)."""
+    rng = _rng(3)
+    T, K, V = 7, 5, 3
+    q, k, v, _, _ = _inputs(rng, T, K, V)
+    g = -rng.uniform(0.05, 0.9, K)
+    S0 = rng.standard_normal((K, V))
+    _, S = orc.unit(q, k, v, np.tile(g, (T, 1)), np.zeros(T), S0)
+    np.testing.assert_allclose(S, np.exp(T * g)[:, None] * S0, rtol=1e-12, atol=1e-15)
+
+
+def pin_write_exactness(orc):
+    """beta = 1, |k| = 1: the updated state reads back v at key k (S_t^T k_t = v_t)
+    for any decay and any previous state, so q_t = k_t gives o_t = scale v_t."""
+    rng = _rng(4)
+    T, K, V, scale = 5, 6, 4, 0.5
+    _, k, v, gk, _ = _inputs(rng, T, K, V)
+    S0 = rng.standard_normal((K, V))
+    o, _ = orc.unit(k, k, v, gk, np.ones(T), S0, scale=scale)
+    np.testing.assert_allclose(o, scale * v, rtol=1e-12, atol=1e-12)
+
+
+def pin_delta_rule_geometry(orc):
+    """One token, |k| = 1: for x orthogonal to k the read-out is the decayed old
+    one, x^T S_1 = x^T Diag(alpha) S0, and at k it moves a fraction beta toward v,
+    k^T S_1 = (1 - beta) k^T Diag(alpha) S0 + beta v^T.  These two facts fix S_1."""
+    rng = _rng(5)
+    K, V = 6, 4
+    q, k, v, gk, beta = _inputs(rng, 1, K, V)
+    S0 = rng.standard_normal((K, V))
+    _, S1 = orc.unit(q, k, v, gk, beta, S0)
+    M = np.exp(gk[0])[:, None] * S0
+    basis = np.linalg.qr(np.column_stack([k[0], rng.standard_normal((K, K - 1))]))[0]
+    for c in range(1, K):
+        x = basis[:, c]
+        np.testing.assert_allclose(x @ S1, x @ M, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(k[0] @ S1, (1 - beta[0]) * (k[0] @ M) + beta[0] * v[0], rtol=1e-11,
+                               atol=1e-12)
+
+
+def pin_affine_in_initial_state(orc):
+    """S_T and o are affine in S0: f(aX + bY) = a f(X) + b f(Y) when a + b = 1."""
+    rng = _rng(6)
+    T, K, V = 9, 5, 4
+    q, k, v, gk, beta = _inputs(rng, T, K, V)
+    X, Y = rng.standard_normal((K, V)), rng.standard_normal((K, V))
+    a, b = 1.7, -0.7
+    oX, SX = orc.unit(q, k, v, gk, beta, X)
+    oY, SY = orc.unit(q, k, v, gk, beta, Y)
+    oZ, SZ = orc.unit(q, k, v, gk, beta, a * X + b * Y)
+    np.testing.assert_allclose(SZ, a * SX + b * SY, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(oZ, a * oX + b * oY, rtol=1e-11, atol=1e-12)
+
+
+def pin_brute_force_tiny(orc):
+    """T <= 8, K = 4, V = 3: explicit matrix products of the definition
+    S_t = (I - beta k k^T) Diag(exp(gk)) S_{t-1} + beta k v^T, o_t = S_t^T (scale q)."""
+    rng = _rng(7)
+    T, K, V, scale = 8, 4, 3, 0.9
+    q, k, v, gk, beta = _inputs(rng, T, K, V)
+    k = k * rng.uniform(0.5, 1.5, (T, 1))    # non-unit keys as well
+    S0 = rng.standard_normal((K, V))
+    o, S = orc.unit(q, k, v, gk, beta, S0, scale=scale)
+    Sref = S0.copy()
+    for t in range(T):
+        P = np.eye(K) - beta[t] * np.outer(k[t], k[t])
+        Sref = P @ np.diag(np.exp(gk[t])) @ Sref + beta[t] * np.outer(k[t], v[t])
+        np.testing.assert_allclose(o[t], Sref.T @ (scale * q[t]), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S, Sref, rtol=1e-12, atol=1e-13)
+
+
+def pin_split_resume(orc):
+    """Running T1 tokens, then T2 tokens from the saved state, equals running
+    T1 + T2 tokens at once (bit-exact in the sequential form)."""
+    rng = _rng(8)
+    T, K, V = 23, 8, 6
+    q, k, v, gk, beta = _inputs(rng, T, K, V)
+    S0 = 0.02 * rng.standard_normal((K, V))
+    o, S = orc.unit(q, k, v, gk, beta, S0)
+    for cut in (1, 8, 16, 22):
+        o1, S1 = orc.unit(q[:cut], k[:cut], v[:cut], gk[:cut], beta[:cut], S0)
+        o2, S2 = orc.unit(q[cut:], k[cut:], v[cut:], gk[cut:], beta[cut:], S1)
+        assert np.array_equal(S2, S)
+        assert np.array_equal(np.concatenate([o1, o2]), o)
+
+
+def pin_chunked_equals_sequential(orc):
+    """The chunked (UT) form equals the sequential form for several chunk sizes,
+    T not a multiple of the chunk, at K = V = 128 and at small odd sizes."""
+    for seed, (T, K, V) in enumerate([(70, 128, 128), (45, 7, 5)]):
+        rng = _rng(20 + seed)
+        q, k, v, gk, beta = _inputs(rng, T, K, V)
+        S0 = 0.02 * rng.standard_normal((K, V))
+        o, S = orc.unit(q, k, v, gk, beta, S0, scale=0.8)
+        for C in (16, 32, 64):
+            oc, Sc = orc.unit(q, k, v, gk, beta, S0, scale=0.8, chunk=C)
+            assert np.abs(oc - o).max() <= 1e-12 * max(1.0, np.abs(o).max())
+            assert np.abs(Sc - S).max() <= 1e-12 * max(1.0, np.abs(S).max())
+
+
+def pin_fold_is_prefix_commit(orc):
+    """Verify leaves the committed state untouched and its outputs are those of
+    the recurrence over the draft; the fold of an accepted prefix a equals
+    committing the first a tokens (bit-exact); a = 0 is a no-op."""
+    rng = _rng(9)
+    B, G, H, K, V = 3, 5, 2, 6, 4
+    q = rng.standard_normal((B, G, H, K))
+    k = rng.standard_normal((B, G, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, G, H, V))
+    gk = -np.log1p(np.exp(rng.standard_normal((B, G, H, K))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, G, H))))
+    S0 = rng.standard_normal((B, H, K, V))
+    S0_copy = S0.copy()
+    o = orc.verify(q, k, v, gk, beta, S0, scale=1.0)
+    assert np.array_equal(S0, S0_copy)
+    accept = np.array([0, 2, G])
+    Sf = orc.fold(k, v, gk, beta, accept, S0)
+    for b in range(B):
+        for h in range(H):
+            ou, _ = orc.unit(q[b, :, h], k[b, :, h], v[b, :, h], gk[b, :, h], beta[b, :, h], S0[b, h])
+            np.testing.assert_allclose(o[b, :, h], ou, rtol=1e-13, atol=1e-14)
+            a = accept[b]
+            _, Sa = orc.unit(q[b, :a, h], k[b, :a, h], v[b, :a, h], gk[b, :a, h], beta[b, :a, h],
+                             S0[b, h])
+            assert np.array_equal(Sf[b, h], Sa)
+
+
+def pin_batches_equal_units(orc):
+    """The packed varlen / decode drivers equal per-unit runs (bit-exact): pins
+    the token offsets, head strides and per-unit state bookkeeping."""
+    rng = _rng(10)
+    H, K, V = 3, 6, 5
+    lens = [3, 1, 7]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = cu[-1]
+    q = rng.standard_normal((T, H, K))
+    k = rng.standard_normal((T, H, K))
+    v = rng.standard_normal((T, H, V))
+    gk = -rng.uniform(0, 1, (T, H, K))
+    beta = rng.uniform(0, 1, (T, H))
+    S0 = rng.standard_normal((len(lens), H, K, V))
+    o, S = orc.prefill_varlen(q, k, v, gk, beta, cu, S0, scale=0.6)
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        for h in range(H):
+            ou, Su = orc.unit(q[sl, h], k[sl, h], v[sl, h], gk[sl, h], beta[sl, h], S0[n, h], scale=0.6)
+            assert np.array_equal(o[sl, h], ou)
+            assert np.array_equal(S[n, h], Su)
+    od, Sd = orc.decode(q[:2], k[:2], v[:2], gk[:2], beta[:2], S0[:2], scale=0.6)
+    for b in range(2):
+        for h in range(H):
+            ou, Su = orc.unit(q[b:b + 1, h], k[b:b + 1, h], v[b:b + 1, h], gk[b:b + 1, h],
+                              beta[b:b + 1, h], S0[b, h], scale=0.6)
+            assert np.array_equal(od[b, h], ou[0])
+            assert np.array_equal(Sd[b, h], Su)
+
+
+PINS = [
+    pin_single_token_closed_form,
+    pin_identity_when_no_write_no_decay,
+    pin_pure_decay_closed_form,
+    pin_write_exactness,
+    pin_delta_rule_geometry,
+    pin_affine_in_initial_state,
+    pin_brute_force_tiny,
+    pin_split_resume,
+    pin_chunked_equals_sequential,
+    pin_fold_is_prefix_commit,
+    pin_batches_equal_units,
+]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin(oracle)
+
+
+def test_chunked_extreme_decay():
+    """Strong decays (cumulative log-decay far below fp32 range over one chunk):
+    the chunked form still equals the sequential one."""
+    rng = _rng(11)
+    T, K, V = 40, 16, 8
+    q, k, v, gk, beta = _inputs(rng, T, K, V, gk_scale=4.0)
+    gk = gk * 6.0
+    S0 = rng.standard_normal((K, V))
+    o, S = oracle.unit(q, k, v, gk, beta, S0)
+    oc, Sc = oracle.unit(q, k, v, gk, beta, S0, chunk=32)
+    assert np.abs(oc - o).max() <= 1e-11 * max(1.0, np.abs(o).max())
+    assert np.abs(Sc - S).max() <= 1e-11 * max(1.0, np.abs(S).max())
+
+
+def test_empty_units():
+    """A zero-length sequence leaves its state unchanged and writes nothing."""
+    rng = _rng(12)
+    H, K, V = 2, 4, 4
+    cu = np.array([0, 0, 3, 3])
+    q = rng.standard_normal((3, H, K))
+    S0 = rng.standard_normal((3, H, K, V))
+    o, S = oracle.prefill_varlen(q, q, rng.standard_normal((3, H, V)), -np.ones((3, H, K)),
+                                 np.ones((3, H)), cu, S0)
+    assert np.array_equal(S[0], S0[0]) and np.array_equal(S[2], S0[2])
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each mutant copy of the oracle source must fail a pin
+# --------------------------------------------------------------------------
+
+MUTANTS = {
+    "decay_dropped": ("double a = exp(gk[i]);", "double a = 1.0;"),
+    "decay_base2": ("double a = exp(gk[i]);", "double a = exp2(gk[i]);"),
+    "decay_on_columns": ("M[(size_t)i * V + j] = a * S[(size_t)i * V + j];",
+                         "M[(size_t)i * V + j] = exp(gk[j % K]) * S[(size_t)i * V + j];"),
+    "delta_sign_flipped": ("- beta * k[i] * kM[j]", "+ beta * k[i] * kM[j]"),
+    "correction_undecayed": ("kM[j] += k[i] * M[(size_t)i * V + j];",
+                             "kM[j] += k[i] * S[(size_t)i * V + j];"),
+    "beta_dropped_on_write": ("+ beta * k[i] * v[j];", "+ k[i] * v[j];"),
+    "scale_dropped": ("double sq = scale * q[i];", "double sq = q[i];"),
+    "readout_transposed": ("o[j] += S[(size_t)i * V + j] * sq;",
+                           "o[j] += S[(size_t)(j % K) * V + (i % V)] * scale * q[j % K];"),
+    "readout_pre_update": ("    if (o) {\n        /* o = S^T (scale q) */",
+                           "    if (o) {\n        for (int i = 0; i < K; ++i) for (int j = 0; j < V; ++j)"
+                           " S[(size_t)i * V + j] = M[(size_t)i * V + j];\n        /* o = S^T (scale q) */"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    old, new = MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "kda_oracle.c")).read()
+    assert old in src, "mutation anchor not found: %s" % name
+    mpath = tmp_path / ("mut_%s.c" % name)
+    mpath.write_text(src.replace(old, new, 1))
+    mut = oracle.load_variant(str(mpath), str(tmp_path / ("mut_%s.so" % name)))
+    failed = []
+    for pin in PINS:
+        try:
+            pin(mut)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, "planted mistake %s passed every pin" % name
