@@ -1,0 +1,507 @@
+"""Benchmark of the KDA state path on GB300.
+
+One JSON line on stdout (rank 0).  A step is one pass of the path over one
+batch of seeded synthetic input with everything resident in HBM:
+
+  varlen (default headline): kda_chunk_prefill over 8 sequences with lengths
+      uniform in [64, 2048] (seed 1), H = 64, bf16, resuming from checkpointed
+      fp32 states; metric = prefill tokens/s.
+  decode:  69 x (copy-on-write restores for 10% of 384 requests, then
+      kda_decode_step on 384 requests x 64 heads over a 512-slot pool).
+  verify:  69 kda_verify_store_inputs launches (64 requests x 8 draft tokens x
+      64 heads) and one kda_replay_fold over all 69 layers.
+
+The decode and verify+fold workloads are measured in the same run and reported
+under "also".  --impl reference times the oracle (fp64 CPU) on the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import kda_inputs as gen  # noqa: E402
+
+KD = VD = 128
+STATE_B = KD * VD * 4
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        inside = [s for t, s in self.samples if t0 <= t <= t1] or [s for _, s in self.samples]
+        sm = [float(s[0]) for s in inside if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            for n, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed(fn, steps, warmup, ws, sampler=None, stream=None):
+    """W warm-up steps, then exactly K timed steps between barrier+synchronize;
+    CUDA events on the launching stream.  Returns ms per step (max over ranks)."""
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    if sampler:
+        sampler.mark()
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, ws)
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def varlen_workload(device, seed=1, H=64):
+    g = gen.make_gen(seed)
+    lengths = gen.varlen_lengths(8, 64, 2048, g)
+    cu = gen.cu_seqlens(lengths)
+    T = int(cu[-1])
+    gd = gen.make_gen(seed + 1000, device)
+    x = gen.token_inputs(T, H, torch.bfloat16, gd, device=device)
+    ck = gen.checkpoint((8, H, KD, VD), gd, device=device)
+    return dict(lengths=lengths, cu=cu, T=T, H=H, x=x, ck=ck, N=8)
+
+
+def algorithmic_prefill_bytes(T, H, N, es=2, init_read=True, snap=False):
+    per_tok = H * (3 * KD * es + VD * es + es + VD * es)   # q, k, gk, v, beta in; o out
+    states = N * H * STATE_B * ((1 if init_read else 0) + 1 + (1 if snap else 0))
+    return T * per_tok + states
+
+
+def bench_varlen(args, ws, sampler):
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    w = varlen_workload(dev)
+    x, N, H, T = w["x"], w["N"], w["H"], w["T"]
+    pool = torch.empty(2 * N, H, KD, VD, device=dev)
+    pool[:N] = w["ck"]
+    cu_d = w["cu"].to(dev)
+    init = torch.arange(N, dtype=torch.int32, device=dev)
+    out = torch.arange(N, 2 * N, dtype=torch.int32, device=dev)
+    o = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
+    cu_h = w["cu"]
+
+    def step():
+        kda.kda_chunk_prefill(x["q"], x["k"], x["v"], x["gk"], x["beta"], cu_d, cu_h, pool, init,
+                              out, o=o)
+
+    ms = timed(step, args.steps, args.warmup, ws, sampler)
+    # end to end: pinned host inputs -> device, prefill, o -> pinned host, every step
+    hx = {n: t.cpu().pin_memory() for n, t in x.items()}
+    dx = {n: torch.empty_like(t) for n, t in x.items()}
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx.values()) + cu_h.numel() * 4
+    d2h = ho.numel() * ho.element_size()
+    cu_pin = cu_h.pin_memory()
+
+    def step_e2e():
+        for n in dx:
+            dx[n].copy_(hx[n], non_blocking=True)
+        cu_d.copy_(cu_pin, non_blocking=True)
+        kda.kda_chunk_prefill(dx["q"], dx["k"], dx["v"], dx["gk"], dx["beta"], cu_d, cu_h, pool,
+                              init, out, o=o)
+        ho.copy_(o, non_blocking=True)
+
+    ms_e2e = timed(step_e2e, max(3, args.steps // 4), 2, ws)
+    alg = algorithmic_prefill_bytes(T, H, N)
+    return dict(ms=ms, ms_e2e=ms_e2e, T=T, H=H, N=N, lengths=w["lengths"], alg_bytes=alg,
+                h2d=h2d, d2h=d2h, launches_per_step=1)
+
+
+def bench_decode(args, ws, layers=69, B=384, H=64, slots=512, cow_frac=0.10, steps=None):
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    g = gen.make_gen(3)
+    perm = gen.slot_permutation(slots, g)
+    ids = perm[:B].to(dev)
+    unused = perm[B:]
+    n_cow = int(cow_frac * B)
+    cow_req = torch.randperm(B, generator=g)[:n_cow]
+    cow_dst = perm[:B][cow_req].to(torch.int32).to(dev)
+    cow_src = unused[torch.randint(0, slots - B, (n_cow,), generator=g)].to(torch.int32).to(dev)
+    gd = gen.make_gen(1003, dev)
+    pools = [gen.checkpoint((slots, H, KD, VD), gd, device=dev) for _ in range(layers)]
+    xs = [gen.token_inputs(B, H, torch.bfloat16, gd, device=dev) for _ in range(layers)]
+    o = torch.empty(B, H, VD, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(layers)]
+    record = {"on": False}
+
+    def step():
+        for l in range(layers):
+            kda.kda_slot_copy([pools[l]], cow_src, cow_dst)
+            x = xs[l]
+            if record["on"]:
+                ev[l][0].record(stream)
+            kda.kda_decode_step(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids, pools[l], o=o)
+            if record["on"]:
+                ev[l][1].record(stream)
+
+    K = steps or max(3, min(args.steps, 10))
+    ms = timed(step, K, max(3, min(args.warmup, 3)), ws)
+    record["on"] = True
+    step()
+    torch.cuda.synchronize()
+    record["on"] = False
+    dec_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    per_unit = 2 * STATE_B + (3 * KD + VD) * 2 + 2 + VD * 2
+    dec_bytes = B * H * per_unit
+    cow_bytes = 2 * n_cow * H * STATE_B
+    del pools, xs
+    torch.cuda.empty_cache()
+    return dict(ms=ms, dec_ms=dec_ms, dec_bytes=dec_bytes, cow_bytes=cow_bytes, B=B, H=H,
+                layers=layers, n_cow=n_cow)
+
+
+def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, steps=None):
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    g = gen.make_gen(4)
+    ids = gen.slot_permutation(slots, g)[:B].to(dev)
+    accept = gen.accept_lengths(B, G, 0.64, g)
+    acc_d = accept.to(dev)
+    gd = gen.make_gen(1004, dev)
+    pools = [gen.checkpoint((slots, H, KD, VD), gd, device=dev) for _ in range(layers)]
+    rings = [kda.make_ring(slots, R, H, torch.bfloat16, dev) for _ in range(layers)]
+    xs = [gen.token_inputs(G, H, torch.bfloat16, gd, device=dev, lead=(B,)) for _ in range(layers)]
+    o = torch.empty(B, G, H, VD, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev_v = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(layers)]
+    ev_f = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    record = {"on": False}
+
+    def step():
+        for l in range(layers):
+            x = xs[l]
+            if record["on"]:
+                ev_v[l][0].record(stream)
+            kda.kda_verify_store_inputs(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids, pools[l],
+                                        rings[l], o=o)
+            if record["on"]:
+                ev_v[l][1].record(stream)
+        if record["on"]:
+            ev_f[0].record(stream)
+        kda.kda_replay_fold(pools, rings, ids, acc_d, max_accept=G)
+        if record["on"]:
+            ev_f[1].record(stream)
+
+    K = steps or max(3, min(args.steps, 10))
+    ms = timed(step, K, max(3, min(args.warmup, 3)), ws)
+    record["on"] = True
+    step()
+    torch.cuda.synchronize()
+    record["on"] = False
+    ver_ms = statistics.median(a.elapsed_time(b) for a, b in ev_v)
+    fold_ms = ev_f[0].elapsed_time(ev_f[1])
+    rec = 2 * KD + 2 * VD + 4 * KD + 4
+    ver_bytes = B * H * (STATE_B + G * (3 * KD * 2 + VD * 2 + 2) + G * VD * 2 + G * rec)
+    acc_sum = int(accept.sum())
+    fold_bytes = layers * H * (2 * STATE_B * int((accept > 0).sum()) + acc_sum * rec)
+    del pools, rings, xs
+    torch.cuda.empty_cache()
+    return dict(ms=ms, ver_ms=ver_ms, fold_ms=fold_ms, ver_bytes=ver_bytes, fold_bytes=fold_bytes,
+                accepted=acc_sum, mean_accept=acc_sum / B, B=B, G=G, layers=layers, H=H)
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleVarlen:
+    """The oracle (fp64, host cores) on a bounded sample of the varlen workload:
+    whole heads (all 8 sequences of a head) of the same-shaped inputs."""
+
+    def __init__(self):
+        import oracle
+        self.oracle = oracle
+        w = varlen_workload("cpu")
+        self.cu = w["cu"].numpy()
+        self.H = w["H"]
+        self.T = int(self.cu[-1])
+        self.x = {n: t.double().numpy() for n, t in w["x"].items()}
+        self.S0 = w["ck"].double().numpy()
+        self.threads = os.cpu_count() or 1
+        # calibrate the per-token cost on the shortest sequence, one thread
+        n0 = int(np.argmin(np.diff(self.cu)))
+        t0 = time.time()
+        self._run([n0], [0], 1)
+        self.sec_per_tok = (time.time() - t0) / max(1, self.cu[n0 + 1] - self.cu[n0])
+
+    def _run(self, seqs, heads, threads):
+        x = self.x
+        self.oracle.prefill_varlen(x["q"], x["k"], x["v"], x["gk"], x["beta"], self.cu, self.S0,
+                                   seqs=seqs, heads=heads, nthreads=threads)
+
+    def heads_for(self, seconds):
+        return max(1, min(self.H, int(seconds * self.threads / (self.sec_per_tok * self.T))))
+
+    def rate(self, n_heads):
+        """tokens/s: token-heads processed / H / wall time."""
+        t0 = time.time()
+        self._run(list(range(8)), list(range(n_heads)), self.threads)
+        dt = time.time() - t0
+        return self.T * n_heads / self.H / dt, dt
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def profile_traffic(kernel_src, summary_name):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (matched by hash)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    h = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()[:12]
+    m_h = re.search(r"source_sha1:\s*([0-9a-f]+)", txt)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_h or not m_t or m_h.group(1) != h:
+        return None
+    return float(m_t.group(1))
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    orc = OracleVarlen()
+    n_heads = orc.heads_for(max(0.2, 120.0 / (args.steps + args.warmup)))
+    rates, secs = [], 0.0
+    for i in range(args.warmup + args.steps):
+        r, dt = orc.rate(n_heads)
+        if i >= args.warmup:
+            rates.append(r)
+            secs += dt
+    v = statistics.mean(rates)
+    desc = ("per step: %d (sequence, head) units (8 sequences x %d heads) = %d token-heads of the "
+            "varlen workload" % (8 * n_heads, n_heads, orc.T * n_heads))
+    line = {"impl": "reference", "metric": "KDA prefill tok/s (varlen chunked prefill)",
+            "value": v, "unit": "tok/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "varlen prefill: 8 seqs, lengths U[64,2048] (seed 1), H=64, "
+                                   "K=V=128, bf16 inputs, fp32 checkpointed states"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": orc.threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-also", action="store_true", help="skip the decode / verify+fold runs")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    # CPU baseline first (before the first GPU call, no fork after CUDA init)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        try:
+            orc = OracleVarlen()
+            nh = orc.heads_for(15.0)
+            r, dt = orc.rate(nh)
+            cpu = {"value": r, "unit": "tok/s", "cores": orc.threads, "kind": "oracle",
+                   "sample": "%d (sequence, head) units (8 sequences x %d of 64 heads), %d "
+                             "token-heads, %.1f s" % (8 * nh, nh, orc.T * nh, dt)}
+        except Exception as e:  # noqa: BLE001
+            cpu = {"value": None, "unit": "tok/s", "cores": None, "kind": "oracle",
+                   "sample": "failed: %s" % e}
+    from kda_state_gb300 import _build
+    _build.build()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    res = bench_varlen(args, ws, sampler)
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+    hbm, _, peak_kind = peaks()
+    ms = res["ms"]
+    value = res["T"] / (ms / 1e3) * ws
+    achieved = res["alg_bytes"] / (ms / 1e3) / 1e9
+    src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_prefill_tc.cu")
+    traffic = profile_traffic(src, "prefill_varlen.md") if os.path.exists(src) else None
+    line = {
+        "metric": "KDA prefill tok/s (varlen chunked prefill)",
+        "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "varlen prefill: 8 seqs, lengths U[64,2048] (seed 1), H=64, K=V=128, "
+                               "bf16 inputs, fp32 states resumed from checkpoints",
+                   "total_tokens": res["T"], "lengths": res["lengths"],
+                   "l2": "inputs larger than L2 (%.2f GB per step)" % (res["alg_bytes"] / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "peak_kind": peak_kind, "kernel": "kda_chunk_prefill",
+                     "algorithmic_bytes_per_launch": res["alg_bytes"]},
+        "e2e": {"value": res["T"] / (res["ms_e2e"] / 1e3) * ws, "unit": "tok/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": sampler.summary() if sampler else None,
+        "cpu_baseline": cpu,
+    }
+    if not args.no_also:
+        also = {}
+        try:
+            d = bench_decode(args, ws)
+            also["decode"] = {
+                "tok_per_s": d["B"] / (d["ms"] / 1e3) * ws, "ms_per_step": d["ms"],
+                "workload": "384 req x 1 tok, H=64, 512-slot pools, 69 layers, %d CoW copies/layer"
+                            % d["n_cow"],
+                "decode_kernel_us": d["dec_ms"] * 1e3,
+                "decode_kernel_GBps": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9,
+                "decode_kernel_frac": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9 / hbm,
+                "step_GBps": (d["dec_bytes"] + d["cow_bytes"]) * d["layers"] / (d["ms"] / 1e3) / 1e9,
+            }
+        except Exception as e:  # noqa: BLE001
+            also["decode"] = {"error": repr(e)}
+        try:
+            v = bench_verify_fold(args, ws)
+            also["verify_fold"] = {
+                "accepted_tok_per_s": v["accepted"] / (v["ms"] / 1e3) * ws,
+                "verified_tok_per_s": v["B"] * v["G"] / (v["ms"] / 1e3) * ws,
+                "ms_per_step": v["ms"], "mean_accept": v["mean_accept"],
+                "workload": "64 req x 8 draft tok, 69 layers, H=64, 128-slot pools, ring 16",
+                "verify_kernel_us": v["ver_ms"] * 1e3,
+                "verify_kernel_GBps": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9,
+                "verify_kernel_frac": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9 / hbm,
+                "fold_kernel_us": v["fold_ms"] * 1e3,
+                "fold_kernel_GBps": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9,
+                "fold_kernel_frac": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9 / hbm,
+            }
+        except Exception as e:  # noqa: BLE001
+            also["verify_fold"] = {"error": repr(e)}
+        line["also"] = also
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * kda.h -- C ABI of the GB300 KDA state library (libkda.so).
+ *
+ * Kimi Delta Attention (KDA) keeps one fp32 K x V recurrent state per
+ * (sequence or request, head) and updates it with the gated delta rule
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(gk_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T (scale * q_t)
+ *
+ * with K = V = 128.  Sources for the shape of the problem: "SGLang and Miles
+ * Add Day-0 Support for Kimi K3" (lmsys.org), sections "Hybrid KDA Memory
+ * Management" (state overwritten in place, slot pools, copy-on-write and
+ * snapshot copies ordered on the forward stream) and "ReplaySSM: raw-input
+ * replay for the KDA state" (verify that never writes the checkpoint, stored
+ * per-step inputs, one fold launch over all layers and heads, bit-identical
+ * state); the Kimi K3 on B200 deployment notes (zdszero.github.io), timeline
+ * entry "FlashKDA" (chunked prefill with a [128, 128] fp32 state) and
+ * "DSPARK and KDA state" (per-slot input ring, power-of-two length at least
+ * 2 (gamma + 1)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Ownership: the caller allocates and owns every buffer.  The library
+ *    allocates no memory, keeps no state between calls and never
+ *    synchronises the device or the stream.
+ *  - Pointers: "device" pointers must be CUDA device (or managed) memory of
+ *    the current device; "host" pointers are read during the call only.
+ *  - Layouts are dense, row-major, in elements of the stated dtype:
+ *      state pool   float  [num_slots][H][K][V]   (row k = key channel)
+ *      q, k, gk     dtype  [tokens][H][K]
+ *      v, o         dtype  [tokens][H][V]
+ *      beta         dtype  [tokens][H]
+ *  - dtype: KDA_DTYPE_BF16 or KDA_DTYPE_FP32 for q, k, v, gk, beta and o; the
+ *    state is always fp32.  gk is the natural-log decay (<= 0 in practice).
+ *  - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All work is enqueued on it, so stream order is the happens-before
+ *    between calls (e.g. a copy-on-write restore before the decode that
+ *    reads the slot).
+ *  - Errors found on the host (null pointer, negative size, K or V other
+ *    than 128, bad dtype, ring length) return a negative kda_status and
+ *    launch nothing.  A failed launch returns KDA_ERR_CUDA.  Errors that
+ *    depend on device data (a slot id, an accept length, cu_seqlens) OR a
+ *    KDA_DEVERR_* bit into *dev_err (if dev_err is not NULL) and skip the
+ *    affected unit; nothing traps.  The caller reads *dev_err after its own
+ *    synchronisation and clears it.
+ *  - Slot ids within one call must be distinct (two units writing one slot
+ *    race); the library does not check this.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,
+    KDA_ERR_UNSUPPORTED = -2,
+    KDA_ERR_CUDA = -3
+} kda_status;
+
+typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 } kda_dtype;
+
+/* Bits OR-ed into *dev_err by kernels. */
+enum {
+    KDA_DEVERR_SLOT_RANGE = 1,   /* a slot id outside [0, num_slots) */
+    KDA_DEVERR_ACCEPT_RANGE = 2, /* an accept length outside [0, max_accept] */
+    KDA_DEVERR_SEQLENS = 4       /* cu_seqlens not monotone or past total_tokens */
+};
+
+/* Largest number of layers (fold) or pools (slot copy) one call takes: the
+ * per-layer pointers travel in the launch parameters. */
+#define KDA_MAX_LAYERS 256
+
+/* Largest number of sequences for which prefill orders its work longest
+ * first; larger batches run in batch order. */
+#define KDA_MAX_LPT_SEQS 2048
+
+/*
+ * ReplaySSM input ring of ONE layer.  Record i of a verify call for the
+ * request in slot s is stored at entry e = (ring_base + i) mod ring_len:
+ *     k     dtype [num_slots][ring_len][H][K]   key as given
+ *     v     dtype [num_slots][ring_len][H][V]   value as given
+ *     decay float [num_slots][ring_len][H][K]   exp(gk) as the kernel computed it
+ *     beta  float [num_slots][ring_len][H]      beta as the kernel read it
+ * One record is 2*128*sizeof(dtype) + 128*4 + 4 bytes (1028 B for bf16),
+ * against 64 KB for a snapshot of the state.  All four pointers are device
+ * memory.  ring_len must be a power of two and at least 2*G.
+ */
+typedef struct {
+    void *k;
+    void *v;
+    float *decay;
+    float *beta;
+    int ring_len;
+    int reserved;
+} kda_ring;
+
+/*
+ * kda_chunk_prefill -- varlen chunked prefill resuming from checkpoints.
+ *
+ * The pages' FlashKDA kernel (Kimi K3 on B200 deployment notes, timeline entry
+ * "FlashKDA"; CuTe rewrite: one CTA per (sequence, head), fp32 [128,128] state
+ * on chip, longest-first ordering) fuses a chunk's work and the state update
+ * into one kernel.  This call does the same for a packed varlen batch.
+ *
+ *   dt              dtype of q, k, v, gk, beta and o
+ *   num_seqs        N >= 0 sequences; total_tokens = cu_seqlens[N]
+ *   H, K, V         heads, key and value dims (K = V = 128)
+ *   q, k, gk        device [total_tokens][H][K]
+ *   v               device [total_tokens][H][V]
+ *   beta            device [total_tokens][H]
+ *   cu_seqlens_dev  device int32 [N+1], sequence n = tokens cu[n] .. cu[n+1]-1
+ *   cu_seqlens_host host int32 [N+1], the same values (required): validated
+ *                   (cu[0] = 0, non-decreasing, cu[N] = total_tokens) and used
+ *                   to order the work longest first; the device copy is still
+ *                   checked per unit (KDA_DEVERR_SEQLENS)
+ *   state_pool      device float [num_slots][H][K][V]
+ *   init_slot       device int32 [N]: initial state slot, or -1 for zeros
+ *   out_slot        device int32 [N]: slot receiving the final state (may equal
+ *                   init_slot: in-place resume)
+ *   snap_slot       device int32 [N] or NULL: if given and >= 0, an extra copy
+ *                   of the final state (the snapshot taken at a chunk boundary)
+ *   o               device [total_tokens][H][V], dtype dt
+ *   scale           multiplies q
+ *   dev_err         device int32 or NULL
+ *   stream          cudaStream_t
+ * bf16 runs the chunked tensor-core kernel; fp32 runs an exact fp32 kernel on
+ * the CUDA cores.  Zero-length sequences copy init to out (or write zeros).
+ */
+KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
+                              const void *q, const void *k, const void *v, const void *gk,
+                              const void *beta, const int32_t *cu_seqlens_dev,
+                              const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
+                              const int32_t *init_slot, const int32_t *out_slot,
+                              const int32_t *snap_slot, void *o, float scale, int32_t *dev_err,
+                              void *stream);
+
+/*
+ * kda_decode_step -- one token per request, state updated in place.
+ *
+ * The working slot is read and overwritten by every forward ("SGLang and Miles
+ * Add Day-0 Support for Kimi K3", "Hybrid KDA Memory Management"); the pages'
+ * fused decode kernel is ladder step P5 ("Kernels").
+ *
+ *   q, k, gk  device [B][H][K];  v, o device [B][H][V];  beta device [B][H]
+ *   slot_ids  device int32 [B], distinct, each in [0, num_slots)
+ *   state_pool device float [num_slots][H][K][V], updated in place
+ * A request whose slot id is out of range is skipped (its o is not written).
+ */
+KDA_API int kda_decode_step(kda_dtype dt, int B, int H, int K, int V, const void *q,
+                            const void *k, const void *v, const void *gk, const void *beta,
+                            const int32_t *slot_ids, float *state_pool, int num_slots, void *o,
+                            float scale, int32_t *dev_err, void *stream);
+
+/*
+ * kda_verify_store_inputs -- speculative verify of G draft tokens.
+ *
+ * Reads each request's committed state and NEVER writes it; emits o for the G
+ * draft positions and stores each step's inputs (k, v, exp(gk), beta) into the
+ * layer's ring ("ReplaySSM: raw-input replay for the KDA state").
+ *
+ *   q, k, gk   device [B][G][H][K];  v, o device [B][G][H][V];  beta [B][G][H]
+ *   slot_ids   device int32 [B]
+ *   state_pool device float [num_slots][H][K][V], read only
+ *   ring       host pointer to this layer's ring descriptor (device buffers)
+ *   ring_base  device int32 [B] or NULL (= 0): ring entry of draft step 0
+ * Requires 1 <= G <= ring->ring_len / 2.
+ */
+KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, int V,
+                                    const void *q, const void *k, const void *v, const void *gk,
+                                    const void *beta, const int32_t *slot_ids,
+                                    const float *state_pool, int num_slots, const kda_ring *ring,
+                                    const int32_t *ring_base, void *o, float scale,
+                                    int32_t *dev_err, void *stream);
+
+/*
+ * kda_replay_fold -- commit the accepted prefix, all layers and heads, one launch.
+ *
+ * For every layer l, request b and head h: load the committed state from
+ * state_pools[l] at slot_ids[b], apply the stored records 0 .. accept_len[b]-1
+ * with the same per-token arithmetic as kda_decode_step, and overwrite the
+ * slot.  The result is bit-identical to accept_len[b] calls of
+ * kda_decode_step on the same inputs.  accept_len 0 leaves the slot untouched.
+ *
+ *   dt          dtype of the rings' k and v
+ *   num_layers  L in [1, KDA_MAX_LAYERS]
+ *   state_pools host array [L] of device pools float [num_slots][H][K][V]
+ *   rings       host array [L] of ring descriptors (same ring_len for all)
+ *   max_accept  upper bound for accept_len (<= ring_len)
+ *   slot_ids    device int32 [B];  accept_len device int32 [B]
+ *   ring_base   device int32 [B] or NULL (= 0)
+ */
+KDA_API int kda_replay_fold(kda_dtype dt, int num_layers, int B, int H, int K, int V,
+                            float *const *state_pools, const kda_ring *rings, int num_slots,
+                            int max_accept, const int32_t *slot_ids, const int32_t *accept_len,
+                            const int32_t *ring_base, int32_t *dev_err, void *stream);
+
+/*
+ * kda_slot_copy -- dst slot <- src slot in every pool, bit-exact.
+ *
+ * The copy-on-write restore and the snapshot of "Hybrid KDA Memory
+ * Management": kernels on the caller's (forward) stream.
+ *
+ *   num_pools   P in [1, KDA_MAX_LAYERS]; pools host array [P] of device pools
+ *   slot_elems  floats per slot (H*K*V), a multiple of 4
+ *   src, dst    device int32 [n]; pairs must not overlap (no slot is both a
+ *               source and a destination in one call)
+ */
+KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems, int num_slots,
+                          const int32_t *src, const int32_t *dst, int n, int32_t *dev_err,
+                          void *stream);
+
+/* Human-readable name of a kda_status value. */
+KDA_API const char *kda_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

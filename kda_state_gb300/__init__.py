@@ -1,0 +1,36 @@
+"""GB300-native KDA (Kimi Delta Attention) recurrent-state library.
+
+The compute runs in hand-written sm_103a CUDA kernels behind the C ABI of
+``libkda.so`` (include/kda.h); this package is the thin Python binding.
+"""
+from .binding import (  # noqa: F401
+    KDA_DEVERR_ACCEPT_RANGE,
+    KDA_DEVERR_SEQLENS,
+    KDA_DEVERR_SLOT_RANGE,
+    KDA_DTYPE_BF16,
+    KDA_DTYPE_FP32,
+    KDA_ERR_CUDA,
+    KDA_ERR_INVALID_ARG,
+    KDA_ERR_UNSUPPORTED,
+    KDA_MAX_LAYERS,
+    KDA_OK,
+    KdaError,
+    RingBuffers,
+    kda_chunk_prefill,
+    kda_decode_step,
+    kda_replay_fold,
+    kda_ring,
+    kda_slot_copy,
+    kda_status_string,
+    kda_verify_store_inputs,
+    lib,
+    make_ring,
+    record_bytes,
+    ring_len_for,
+    state_bytes,
+)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from ._build import build as _b
+    return _b(force=force, verbose=verbose)

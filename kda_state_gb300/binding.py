@@ -1,0 +1,231 @@
+"""ctypes binding of libkda.so: the C entry points under the same names.
+
+Argument marshalling only -- every step of the KDA path runs in the library's
+CUDA kernels.  Tensors are torch tensors on the current CUDA device (PyTorch
+supplies device memory and streams); shapes follow include/kda.h.  If the
+library is missing the calls raise: there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_CUDA = -3
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_FP32 = 1
+KDA_DEVERR_SLOT_RANGE = 1
+KDA_DEVERR_ACCEPT_RANGE = 2
+KDA_DEVERR_SEQLENS = 4
+KDA_MAX_LAYERS = 256
+K_DIM = 128
+V_DIM = 128
+
+_DT = {torch.bfloat16: KDA_DTYPE_BF16, torch.float32: KDA_DTYPE_FP32}
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__("%s failed: %s (%d)" % (fn, kda_status_string(status), status))
+        self.status = status
+
+
+class kda_ring(ctypes.Structure):
+    """Mirror of the C struct ``kda_ring`` (one layer's ReplaySSM input ring)."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("decay", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p), ("ring_len", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkda.so (built by ``kda_state_gb300._build.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libkda.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, ip = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        L.kda_chunk_prefill.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, ip, vp, i, ip, ip,
+                                        ip, vp, f, ip, vp]
+        L.kda_decode_step.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i, vp, f, ip, vp]
+        L.kda_verify_store_inputs.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i,
+                                              ctypes.POINTER(kda_ring), ip, vp, f, ip, vp]
+        L.kda_replay_fold.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_void_p),
+                                      ctypes.POINTER(kda_ring), i, i, ip, ip, ip, ip, vp]
+        L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
+                                    i, ip, vp]
+        for fn in ("kda_chunk_prefill", "kda_decode_step", "kda_verify_store_inputs",
+                   "kda_replay_fold", "kda_slot_copy"):
+            getattr(L, fn).restype = ctypes.c_int
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn, status):
+    if status != KDA_OK:
+        raise KdaError(fn, status)
+
+
+def _dt(t):
+    if t.dtype not in _DT:
+        raise TypeError("unsupported dtype %s (bf16 or fp32)" % t.dtype)
+    return _DT[t.dtype]
+
+
+# ---------------------------------------------------------------------------
+# ReplaySSM ring helpers
+# ---------------------------------------------------------------------------
+
+def ring_len_for(gamma: int) -> int:
+    """Ring length for gamma draft tokens: the smallest power of two that is at
+    least 2 (gamma + 1) (gamma = 5 -> 12 -> 16)."""
+    need = 2 * (int(gamma) + 1)
+    r = 1
+    while r < need:
+        r <<= 1
+    return r
+
+
+def state_bytes(K: int = K_DIM, V: int = V_DIM) -> int:
+    """Bytes of one (request, layer, head) fp32 state: 64 KB at K = V = 128."""
+    return K * V * 4
+
+
+def record_bytes(dtype=torch.bfloat16, K: int = K_DIM, V: int = V_DIM) -> int:
+    """Bytes of one stored ring record: k and v in the input dtype, exp(gk) and
+    beta in fp32 (1028 B for bf16 at K = V = 128)."""
+    es = torch.tensor([], dtype=dtype).element_size()
+    return K * es + V * es + K * 4 + 4
+
+
+@dataclass
+class RingBuffers:
+    """One layer's ring: k, v [num_slots, R, H, K|V] (input dtype), decay
+    [num_slots, R, H, K] and beta [num_slots, R, H] (fp32)."""
+    k: torch.Tensor
+    v: torch.Tensor
+    decay: torch.Tensor
+    beta: torch.Tensor
+
+    @property
+    def ring_len(self) -> int:
+        return self.k.shape[1]
+
+    def descriptor(self) -> kda_ring:
+        return kda_ring(self.k.data_ptr(), self.v.data_ptr(), self.decay.data_ptr(),
+                        self.beta.data_ptr(), self.ring_len, 0)
+
+
+def make_ring(num_slots: int, ring_len: int, H: int, dtype=torch.bfloat16, device="cuda",
+              K: int = K_DIM, V: int = V_DIM) -> RingBuffers:
+    return RingBuffers(torch.zeros(num_slots, ring_len, H, K, dtype=dtype, device=device),
+                       torch.zeros(num_slots, ring_len, H, V, dtype=dtype, device=device),
+                       torch.zeros(num_slots, ring_len, H, K, dtype=torch.float32, device=device),
+                       torch.zeros(num_slots, ring_len, H, dtype=torch.float32, device=device))
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def kda_chunk_prefill(q, k, v, gk, beta, cu_seqlens, cu_seqlens_host, state_pool, init_slot,
+                      out_slot, snap_slot=None, o=None, scale: float = 1.0, dev_err=None,
+                      stream=None):
+    """q/k/gk [T, H, K], v [T, H, V], beta [T, H] on the device; cu_seqlens int32
+    [N+1] on the device and its host copy; state_pool fp32 [slots, H, K, V];
+    init_slot / out_slot / snap_slot int32 [N] on the device.  Returns o."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    N = host.numel() - 1
+    if o is None:
+        o = torch.empty(T, H, V, dtype=q.dtype, device=q.device)
+    hp = host.numpy().ctypes.data_as(ctypes.c_void_p)
+    _check("kda_chunk_prefill", lib().kda_chunk_prefill(
+        _dt(q), N, T, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(cu_seqlens), hp,
+        _p(state_pool), state_pool.shape[0], _p(init_slot), _p(out_slot), _p(snap_slot), _p(o),
+        float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
+def kda_decode_step(q, k, v, gk, beta, slot_ids, state_pool, o=None, scale: float = 1.0,
+                    dev_err=None, stream=None):
+    """q/k/gk [B, H, K], v [B, H, V], beta [B, H]; slot_ids int32 [B].  Updates the
+    pool in place and returns o [B, H, V]."""
+    B, H, K = q.shape
+    V = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, H, V, dtype=q.dtype, device=q.device)
+    _check("kda_decode_step", lib().kda_decode_step(
+        _dt(q), B, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(slot_ids), _p(state_pool),
+        state_pool.shape[0], _p(o), float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
+def kda_verify_store_inputs(q, k, v, gk, beta, slot_ids, state_pool, ring: RingBuffers,
+                            ring_base=None, o=None, scale: float = 1.0, dev_err=None, stream=None):
+    """q/k/gk [B, G, H, K], v [B, G, H, V], beta [B, G, H]; reads the pool, never
+    writes it; stores the G records into ``ring``.  Returns o [B, G, H, V]."""
+    B, G, H, K = q.shape
+    V = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, G, H, V, dtype=q.dtype, device=q.device)
+    desc = ring.descriptor()
+    _check("kda_verify_store_inputs", lib().kda_verify_store_inputs(
+        _dt(q), B, G, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(slot_ids),
+        _p(state_pool), state_pool.shape[0], ctypes.byref(desc), _p(ring_base), _p(o),
+        float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
+def kda_replay_fold(state_pools, rings, slot_ids, accept_len, max_accept: int, ring_base=None,
+                    dev_err=None, stream=None):
+    """Fold the accepted prefixes of every layer in one launch.  state_pools: list
+    of L fp32 pools [slots, H, K, V]; rings: list of L RingBuffers."""
+    L = len(state_pools)
+    if L != len(rings) or L == 0:
+        raise ValueError("state_pools and rings must be non-empty lists of equal length")
+    S, H, K, V = state_pools[0].shape
+    B = slot_ids.numel()
+    ptrs = (ctypes.c_void_p * L)(*[p.data_ptr() for p in state_pools])
+    descs = (kda_ring * L)(*[r.descriptor() for r in rings])
+    _check("kda_replay_fold", lib().kda_replay_fold(
+        _DT[rings[0].k.dtype], L, B, H, K, V, ptrs, descs, S, int(max_accept), _p(slot_ids),
+        _p(accept_len), _p(ring_base), _p(dev_err), _stream(stream)))
+
+
+def kda_slot_copy(pools, src, dst, dev_err=None, stream=None):
+    """dst[i] <- src[i] in every pool of the list (int32 device index tensors)."""
+    P = len(pools)
+    ptrs = (ctypes.c_void_p * P)(*[p.data_ptr() for p in pools])
+    slot_elems = pools[0][0].numel()
+    _check("kda_slot_copy", lib().kda_slot_copy(
+        P, ptrs, slot_elems, pools[0].shape[0], _p(src), _p(dst), src.numel(), _p(dev_err),
+        _stream(stream)))

@@ -1,0 +1,166 @@
+// C entry points of libkda.so: argument validation, launch parameters, and the
+// launch on the caller's stream.  No allocation, no synchronisation, no state.
+// The contract of every function is documented in include/kda.h.
+#include <math.h>
+#include <string.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+bool dtype_ok(int dt) { return dt == KDA_DTYPE_BF16 || dt == KDA_DTYPE_FP32; }
+bool dims_ok(int K, int V) { return K == 128 && V == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+KDA_API const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
+                              const void *q, const void *k, const void *v, const void *gk,
+                              const void *beta, const int32_t *cu_seqlens_dev,
+                              const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
+                              const int32_t *init_slot, const int32_t *out_slot,
+                              const int32_t *snap_slot, void *o, float scale, int32_t *dev_err,
+                              void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H < 1 || num_slots < 1 || !isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens_dev || !cu_seqlens_host || !state_pool || !init_slot || !out_slot)
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !gk || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    if ((long long)num_seqs * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens)
+        return KDA_ERR_INVALID_ARG;
+    for (int n = 0; n < num_seqs; ++n)
+        if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+
+    kda::PrefillArgs a;
+    a.dt = dt; a.N = num_seqs; a.T_total = total_tokens; a.H = H; a.num_slots = num_slots;
+    a.q = q; a.k = k; a.v = v; a.gk = gk; a.beta = beta;
+    a.cu = cu_seqlens_dev; a.cu_host = cu_seqlens_host;
+    a.pool = state_pool; a.init_slot = init_slot; a.out_slot = out_slot; a.snap_slot = snap_slot;
+    a.o = o; a.scale = scale; a.err = dev_err;
+    cudaStream_t s = (cudaStream_t)stream;
+    return from_cuda(kda::launch_prefill_recurrent(a, s));
+}
+
+KDA_API int kda_decode_step(kda_dtype dt, int B, int H, int K, int V, const void *q,
+                            const void *k, const void *v, const void *gk, const void *beta,
+                            const int32_t *slot_ids, float *state_pool, int num_slots, void *o,
+                            float scale, int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || num_slots < 1 || !isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !gk || !beta || !slot_ids || !state_pool || !o)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::DecodeArgs a;
+    a.dt = dt; a.B = B; a.H = H; a.num_slots = num_slots;
+    a.q = q; a.k = k; a.v = v; a.gk = gk; a.beta = beta;
+    a.slot_ids = slot_ids; a.pool = state_pool; a.o = o; a.scale = scale; a.err = dev_err;
+    return from_cuda(kda::launch_decode(a, (cudaStream_t)stream));
+}
+
+static bool ring_ok(const kda_ring *r, int G) {
+    if (!r || !r->k || !r->v || !r->decay || !r->beta) return false;
+    const int R = r->ring_len;
+    if (R < 2 || (R & (R - 1)) != 0) return false;
+    return G >= 1 && 2 * G <= R;
+}
+
+KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, int V,
+                                    const void *q, const void *k, const void *v, const void *gk,
+                                    const void *beta, const int32_t *slot_ids,
+                                    const float *state_pool, int num_slots, const kda_ring *ring,
+                                    const int32_t *ring_base, void *o, float scale,
+                                    int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || num_slots < 1 || G < 1 || G > 64 || !isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (!ring_ok(ring, G)) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !gk || !beta || !slot_ids || !state_pool || !o)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::VerifyArgs a;
+    a.dt = dt; a.B = B; a.G = G; a.H = H; a.num_slots = num_slots; a.ring_len = ring->ring_len;
+    a.q = q; a.k = k; a.v = v; a.gk = gk; a.beta = beta;
+    a.slot_ids = slot_ids; a.ring_base = ring_base; a.pool = state_pool;
+    a.rk = ring->k; a.rv = ring->v; a.rdecay = ring->decay; a.rbeta = ring->beta;
+    a.o = o; a.scale = scale; a.err = dev_err;
+    return from_cuda(kda::launch_verify(a, (cudaStream_t)stream));
+}
+
+KDA_API int kda_replay_fold(kda_dtype dt, int num_layers, int B, int H, int K, int V,
+                            float *const *state_pools, const kda_ring *rings, int num_slots,
+                            int max_accept, const int32_t *slot_ids, const int32_t *accept_len,
+                            const int32_t *ring_base, int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (num_layers < 1 || num_layers > KDA_MAX_LAYERS || B < 0 || H < 1 || num_slots < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (!state_pools || !rings) return KDA_ERR_INVALID_ARG;
+    const int R = rings[0].ring_len;
+    if (max_accept < 1 || max_accept > R || max_accept > 64) return KDA_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l) {
+        const kda_ring &r = rings[l];
+        if (!state_pools[l] || !aligned16(state_pools[l])) return KDA_ERR_INVALID_ARG;
+        if (!r.k || !r.v || !r.decay || !r.beta || r.ring_len != R || R < 2 || (R & (R - 1)))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if (B == 0) return KDA_OK;
+    if (!slot_ids || !accept_len) return KDA_ERR_INVALID_ARG;
+    if ((long long)num_layers * B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::FoldParams p;   // ~10 KB, copied into the launch parameters
+    kda::FoldParams *pp = &p;
+    pp->L = num_layers; pp->B = B; pp->H = H; pp->num_slots = num_slots;
+    pp->max_accept = max_accept; pp->ring_len = R;
+    pp->slot_ids = slot_ids; pp->accept = accept_len; pp->ring_base = ring_base; pp->err = dev_err;
+    for (int l = 0; l < num_layers; ++l) {
+        pp->layer[l].pool = state_pools[l];
+        pp->layer[l].rk = rings[l].k;
+        pp->layer[l].rv = rings[l].v;
+        pp->layer[l].rdecay = rings[l].decay;
+        pp->layer[l].rbeta = rings[l].beta;
+    }
+    return from_cuda(kda::launch_fold(p, dt, (cudaStream_t)stream));
+}
+
+KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems, int num_slots,
+                          const int32_t *src, const int32_t *dst, int n, int32_t *dev_err,
+                          void *stream) {
+    if (num_pools < 1 || num_pools > KDA_MAX_LAYERS || num_slots < 1 || n < 0 || !pools)
+        return KDA_ERR_INVALID_ARG;
+    if (slot_elems == 0 || (slot_elems & 3u) != 0) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < num_pools; ++i)
+        if (!pools[i] || !aligned16(pools[i])) return KDA_ERR_INVALID_ARG;
+    if (n == 0) return KDA_OK;
+    if (!src || !dst) return KDA_ERR_INVALID_ARG;
+    kda::CopyParams p;
+    memset(&p, 0, sizeof(p));
+    p.P = num_pools; p.n = n; p.num_slots = num_slots; p.slot_elems = slot_elems;
+    p.src = src; p.dst = dst; p.err = dev_err;
+    for (int i = 0; i < num_pools; ++i) p.pool[i] = pools[i];
+    return from_cuda(kda::launch_slot_copy(p, (cudaStream_t)stream));
+}
+
+}  // extern "C"

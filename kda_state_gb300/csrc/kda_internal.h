@@ -1,0 +1,78 @@
+// Internal launch interface between the C entry points (kda_api.cu) and the
+// kernel translation units.  Host-side only; no device code here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+struct DecodeArgs {
+    int dt, B, H, num_slots;
+    const void *q, *k, *v, *gk, *beta;
+    const int32_t *slot_ids;
+    float *pool;
+    void *o;
+    float scale;
+    int32_t *err;
+};
+
+struct VerifyArgs {
+    int dt, B, G, H, num_slots, ring_len;
+    const void *q, *k, *v, *gk, *beta;
+    const int32_t *slot_ids, *ring_base;
+    const float *pool;
+    void *rk, *rv;
+    float *rdecay, *rbeta;
+    void *o;
+    float scale;
+    int32_t *err;
+};
+
+// One layer of a fold: its state pool and ring buffers.
+struct FoldLayer {
+    float *pool;
+    void *rk, *rv;
+    float *rdecay, *rbeta;
+};
+
+struct FoldParams {
+    int L, B, H, num_slots, max_accept, ring_len;
+    const int32_t *slot_ids, *accept, *ring_base;
+    int32_t *err;
+    FoldLayer layer[KDA_MAX_LAYERS];
+};
+
+struct CopyParams {
+    int P, n, num_slots, chunks_per_copy;
+    size_t slot_elems;
+    const int32_t *src, *dst;
+    int32_t *err;
+    float *pool[KDA_MAX_LAYERS];
+};
+
+struct PrefillArgs {
+    int dt, N, T_total, H, num_slots;
+    const void *q, *k, *v, *gk, *beta;
+    const int32_t *cu;            // device
+    const int32_t *cu_host;       // host (validated)
+    float *pool;
+    const int32_t *init_slot, *out_slot, *snap_slot;
+    void *o;
+    float scale;
+    int32_t *err;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s);
+cudaError_t launch_fold(const FoldParams &p, int dt, cudaStream_t s);
+cudaError_t launch_slot_copy(const CopyParams &p, cudaStream_t s);
+// Exact fp32 CUDA-core prefill (token by token, state in registers).
+cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t s);
+// Chunked tensor-core prefill (bf16 inputs).
+cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,138 @@
+"""Host-side checks that need no GPU: the library loads, exports every entry
+point include/kda.h declares, rejects bad arguments before launching anything,
+and its layout helpers agree with the sizes the pages print."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kda_state_gb300 import _build
+    _build.build()
+    import kda_state_gb300 as kda
+    return kda.lib()
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "kda.h")).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]*?\b(kda_\w+)\s*\(", hdr)))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ("kda_chunk_prefill", "kda_decode_step", "kda_verify_store_inputs",
+              "kda_replay_fold", "kda_slot_copy", "kda_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_symbols():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    import kda_state_gb300 as kda
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert kda.kda_status_string(-1) == "KDA_ERR_INVALID_ARG"
+    assert kda.kda_status_string(-2) == "KDA_ERR_UNSUPPORTED"
+    assert kda.kda_status_string(-3) == "KDA_ERR_CUDA"
+
+
+FAKE = ctypes.c_void_p(4096)   # never dereferenced: every call below fails validation first
+
+
+def test_decode_rejects_before_launch(L):
+    # K != 128
+    assert L.kda_decode_step(0, 4, 2, 64, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE,
+                             1.0, None, None) == -2
+    # bad dtype
+    assert L.kda_decode_step(7, 4, 2, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE,
+                             1.0, None, None) == -2
+    # null pointer
+    assert L.kda_decode_step(0, 4, 2, 128, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE,
+                             1.0, None, None) == -1
+    # misaligned pool
+    assert L.kda_decode_step(0, 4, 2, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             ctypes.c_void_p(4100), 8, FAKE, 1.0, None, None) == -1
+    # non-finite scale
+    assert L.kda_decode_step(0, 4, 2, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE,
+                             float("nan"), None, None) == -1
+    # empty batch: nothing to do
+    assert L.kda_decode_step(0, 0, 2, 128, 128, None, None, None, None, None, None, None, 8, None,
+                             1.0, None, None) == 0
+
+
+def _cu(vals):
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr
+
+
+def test_prefill_rejects_bad_cu_seqlens(L):
+    args = lambda cu, N, T: (0, N, T, 2, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cu, FAKE, 4,
+                             FAKE, FAKE, None, FAKE, 1.0, None, None)
+    assert L.kda_chunk_prefill(*args(_cu([0, 5, 3]), 2, 3)) == -1     # decreasing
+    assert L.kda_chunk_prefill(*args(_cu([1, 5, 9]), 2, 9)) == -1     # cu[0] != 0
+    assert L.kda_chunk_prefill(*args(_cu([0, 5, 9]), 2, 10)) == -1    # cu[N] != total
+    assert L.kda_chunk_prefill(*args(None, 2, 9)) == -1               # host copy required
+    assert L.kda_chunk_prefill(*(0, 0, 0, 2, 128, 128) + (None,) * 5 + (FAKE, _cu([0]), FAKE, 4,
+                               FAKE, FAKE, None, None, 1.0, None, None)) == 0
+    assert L.kda_chunk_prefill(*(0, 1, 4, 2, 128, 96) + (FAKE,) * 6 + (_cu([0, 4]), FAKE, 4,
+                               FAKE, FAKE, None, FAKE, 1.0, None, None)) == -2
+
+
+def test_verify_and_fold_ring_rules(L):
+    import kda_state_gb300 as kda
+    ring = kda.kda_ring(4096, 4096, 4096, 4096, 12, 0)           # not a power of two
+    assert L.kda_verify_store_inputs(0, 2, 5, 2, 128, 128, *(FAKE,) * 6, FAKE, 4, ctypes.byref(ring),
+                                     None, FAKE, 1.0, None, None) == -1
+    ring.ring_len = 8                                              # 2 * G > R for G = 5
+    assert L.kda_verify_store_inputs(0, 2, 5, 2, 128, 128, *(FAKE,) * 6, FAKE, 4, ctypes.byref(ring),
+                                     None, FAKE, 1.0, None, None) == -1
+    rings = (kda.kda_ring * 2)(kda.kda_ring(4096, 4096, 4096, 4096, 16, 0),
+                               kda.kda_ring(4096, 4096, 4096, 4096, 8, 0))   # ring lengths differ
+    pools = (ctypes.c_void_p * 2)(4096, 4096)
+    assert L.kda_replay_fold(0, 2, 2, 2, 128, 128, pools, rings, 4, 8, FAKE, FAKE, None, None,
+                             None) == -1
+    rings[1].ring_len = 16
+    assert L.kda_replay_fold(0, 2, 2, 2, 128, 128, pools, rings, 4, 17, FAKE, FAKE, None, None,
+                             None) == -1                             # max_accept > ring_len
+    assert L.kda_replay_fold(0, 0, 2, 2, 128, 128, pools, rings, 4, 8, FAKE, FAKE, None, None,
+                             None) == -1                             # no layers
+    assert L.kda_replay_fold(0, 2, 0, 2, 128, 128, pools, rings, 4, 8, None, None, None, None,
+                             None) == 0                              # empty batch
+
+
+def test_slot_copy_rejects(L):
+    pools = (ctypes.c_void_p * 1)(4096)
+    assert L.kda_slot_copy(1, pools, 6, 4, FAKE, FAKE, 1, None, None) == -1      # not multiple of 4
+    assert L.kda_slot_copy(0, pools, 16, 4, FAKE, FAKE, 1, None, None) == -1     # no pools
+    assert L.kda_slot_copy(257, pools, 16, 4, FAKE, FAKE, 1, None, None) == -1   # too many pools
+    assert L.kda_slot_copy(1, pools, 16, 4, None, None, 0, None, None) == 0      # nothing to copy
+
+
+def test_layout_helpers_match_page_sizes():
+    import kda_state_gb300 as kda
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "page_sizes.json")))
+    sb = kda.state_bytes()
+    assert sb == g["state_bytes_per_request_layer_head"]["value"]
+    rb = kda.record_bytes(torch.bfloat16)
+    e = g["raw_input_record_bytes"]
+    assert abs(rb - e["value"]) <= e["rel_tol"] * e["value"]
+    e = g["draft_window_snapshot_bytes"]
+    assert e["gamma_plus_1"] * sb == e["value"]
+    e = g["draft_window_ring_bytes"]
+    assert abs(e["ring_len"] * rb - e["value"]) <= e["rel_tol"] * e["value"]
+    assert 30 <= g["draft_window_snapshot_bytes"]["value"] / (e["ring_len"] * rb) <= 34
+    e = g["ring_len_rule"]
+    assert kda.ring_len_for(e["gamma"]) == e["value"]
+    assert [kda.ring_len_for(x) for x in (0, 1, 3, 7)] == [2, 4, 8, 16]
+    for key in ("state_read_per_request_step_bytes", "state_per_request_tp8_bytes"):
+        e = g[key]
+        assert abs(e["layers"] * e["heads"] * sb - e["value"]) <= e["rel_tol"] * e["value"]
