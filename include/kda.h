@@ -75,7 +75,14 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 } kda_dtype;
 enum {
     KDA_DEVERR_SLOT_RANGE = 1,   /* a slot id outside [0, num_slots) */
     KDA_DEVERR_ACCEPT_RANGE = 2, /* an accept length outside [0, max_accept] */
-    KDA_DEVERR_SEQLENS = 4       /* cu_seqlens not monotone or past total_tokens */
+    KDA_DEVERR_SEQLENS = 4,      /* cu_seqlens not monotone or past total_tokens */
+    KDA_DEVERR_RANGE = 8,        /* chunked prefill: a key channel's log-decay summed over half a
+                                    chunk (32 tokens) is below -85, or a chunk intermediate
+                                    (state, W, U) exceeds 60000 in magnitude: outside what the
+                                    kernel's operand formats represent; that unit's outputs and
+                                    state are not valid */
+    KDA_DEVERR_TIMEOUT = 16      /* a kernel's bounded wait on its own copies gave up (the unit
+                                    is abandoned, its slot is not written) */
 };
 
 /* Largest number of layers (fold) or pools (slot copy) one call takes: the

@@ -5,6 +5,8 @@ The compute runs in hand-written sm_103a CUDA kernels behind the C ABI of
 """
 from .binding import (  # noqa: F401
     KDA_DEVERR_ACCEPT_RANGE,
+    KDA_DEVERR_RANGE,
+    KDA_DEVERR_TIMEOUT,
     KDA_DEVERR_SEQLENS,
     KDA_DEVERR_SLOT_RANGE,
     KDA_DTYPE_BF16,

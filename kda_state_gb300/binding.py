@@ -25,6 +25,8 @@ KDA_DTYPE_FP32 = 1
 KDA_DEVERR_SLOT_RANGE = 1
 KDA_DEVERR_ACCEPT_RANGE = 2
 KDA_DEVERR_SEQLENS = 4
+KDA_DEVERR_RANGE = 8
+KDA_DEVERR_TIMEOUT = 16
 KDA_MAX_LAYERS = 256
 K_DIM = 128
 V_DIM = 128

@@ -56,6 +56,13 @@ KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int 
     a.pool = state_pool; a.init_slot = init_slot; a.out_slot = out_slot; a.snap_slot = snap_slot;
     a.o = o; a.scale = scale; a.err = dev_err;
     cudaStream_t s = (cudaStream_t)stream;
+    if (dt == KDA_DTYPE_BF16) {
+        // the tensor-core kernel stages q, k, v, gk with TMA and stores o in 16-byte vectors
+        if (total_tokens > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+                                 !aligned16(gk) || !aligned16(o)))
+            return KDA_ERR_INVALID_ARG;
+        return from_cuda(kda::launch_prefill_chunked(a, s));
+    }
     return from_cuda(kda::launch_prefill_recurrent(a, s));
 }
 

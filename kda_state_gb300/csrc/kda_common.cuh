@@ -30,7 +30,13 @@ constexpr int CTA_THREADS = 256;
 constexpr int CTA_WARPS = CTA_THREADS / 32;
 constexpr int ROWS_PER_WARP = KD / CTA_WARPS;  // 16 rows of the state per warp
 
-enum { DEVERR_SLOT_RANGE = 1, DEVERR_ACCEPT_RANGE = 2, DEVERR_SEQLENS = 4 };
+enum {
+    DEVERR_SLOT_RANGE = 1,
+    DEVERR_ACCEPT_RANGE = 2,
+    DEVERR_SEQLENS = 4,
+    DEVERR_RANGE = 8,
+    DEVERR_TIMEOUT = 16
+};
 
 __device__ __forceinline__ void report(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);

@@ -1,0 +1,760 @@
+// Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One CTA (512 threads) per (sequence, head) unit walks the sequence in chunks
+// of C = 64 tokens with the fp32 128 x 128 state held in registers across
+// chunks; every chunk-sized contraction runs as a tcgen05.mma (bf16 operands
+// in shared memory, fp32 accumulators in TMEM).  The pages' FlashKDA fuses a
+// chunk's work and the state update into one kernel with intermediates on
+// chip (Kimi K3 on B200 deployment notes, timeline entry "FlashKDA"); its CuTe
+// rewrite keeps the state on chip and issues the longest sequences first.  Both
+// ideas are kept here; the chunk size, the state placement (registers, not
+// TMEM) and the work split are this kernel's own.
+//
+// Chunk algebra (derived from the recurrence
+//     S_t = (I - b_t k_t k_t^T) Diag(exp(gk_t)) S_{t-1} + b_t k_t v_t^T,  o_t = S_t^T q_t
+// by unrolling it over the chunk).  With G_r = sum_{j<=r} gk_j per key channel,
+// S0 the state entering the chunk and the last row's G_L:
+//     A[r][j]  = b_r <k_r, exp(G_r - G_j) . k_j>  (j < r),  T = (I + A)^-1
+//     W        = T Diag(b) (K . exp(G)),   U~ = T Diag(b) V
+//     U        = U~ - W S0
+//     O        = (Q . exp(G)) S0 + Aqk U,  Aqk[r][j] = <q_r, exp(G_r - G_j) . k_j> (j <= r)
+//     S_L      = Diag(exp(G_L)) S0 + (K . exp(G_L - G))^T U
+// The pairwise factors exp(G_r - G_j) are split as exp(G_r - G_ref) *
+// exp(G_ref - G_j) around the chunk's middle row, which keeps both factors in
+// fp32 range while the decay summed over half a chunk stays above -85 (else
+// the unit reports KDA_DEVERR_RANGE).
+//
+// Per chunk, five groups of MMAs (M = 128 throughout; shared-memory operands
+// in the 128-byte-swizzled canonical layouts):
+//   G1  [Kf; Qr] (128x128) x Kb^T           -> TMEM cols [0,64):   A (rows 0-63), Aqk (64-127)
+//   G2  [T Diag(b); 0] (128x64) x [K~ | V]  -> cols [0,128): W,  cols [128,256): U~
+//   G3  [-W; Q~] (128x128) x S0 (+=)        -> cols [128,256): U (rows 0-63), Q~ S0 (64-127)
+//   G4a [0; Aqk] (128x64) x U (+=)          -> cols [128,256): rows 64-127 become O
+//   G4b (K . exp(G_L - G))^T (128x64) x U   -> cols [0,128): the state increment
+// Operand precision: the Gram factors span exp(+-26) and need bf16's range,
+// so G1 runs as three bf16 products (hi*hi + lo*hi + hi*lo of a hi/lo split,
+// ~16-bit significands); G2 takes V as given (bf16); the operands of G3 and G4
+// are bounded (|.| <= 1 for the decayed q, k and Aqk; U, W and S are checked
+// against 60000) and use fp16's 11-bit significand.  Rounding all operands to
+// bf16 instead gives 3e-2 x RMS on o, fp16 + split G1 about 3e-3.
+// CUDA cores do the cumulative decays, the exponentials, the 64x64 unit-lower
+// triangular inverse (16x16 blocks), the TMEM read-outs and the fp32 state
+// update.  All waits are bounded; a wait that gives up reports
+// KDA_DEVERR_TIMEOUT, frees TMEM and abandons the unit.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace tc {
+
+constexpr int C = 64;              // chunk length
+constexpr int NT = 512;            // threads per CTA
+constexpr int AS = 68;             // row stride (floats) of the fp32 A scratch
+
+// Shared-memory map (byte offsets from a 1024-aligned base).  Region R1
+// [0, 96K) holds the G1 operands from the end of the prep to the end of G1,
+// then the next chunk's raw q, k, gk (TMA), the triangular-solve scratch and
+// the [T Diag(b); 0; Aqk] tile.  The prep reads its raw tiles into registers
+// before it overwrites R1.
+constexpr uint32_t OP_A1H = 0;         // [Kf; Qr] hi, bf16, 128 rows x 128 ch, K-major A
+constexpr uint32_t OP_A1L = 32768;     // [Kf; Qr] lo
+constexpr uint32_t OP_B1H = 65536;     // Kb hi, bf16, 64 rows x 128 ch, K-major B
+constexpr uint32_t OP_B1L = 81920;     // Kb lo
+constexpr uint32_t RAW_Q = 0;          // 64 tokens x 128 ch bf16, 2 boxes of 64 ch (TMA)
+constexpr uint32_t RAW_K = 16384;
+constexpr uint32_t RAW_G = 32768;
+constexpr uint32_t SCR_A = 49152;      // fp32 A [64][AS]
+constexpr uint32_t SCR_R = SCR_A + 64 * AS * 4;   // fp32 block products, 3 x 256
+constexpr uint32_t OP_TBZ = 69632;     // rows 0-63 T Diag(b) (bf16), 64-127 zero, 128-191 Aqk (fp16)
+constexpr uint32_t R1_END = 98304;
+constexpr uint32_t RAW_V = 98304;      // v, bf16, also the MN-major B operand of U~ = T Diag(b) V
+constexpr uint32_t OP_KT = 114688;     // K . exp(G), bf16, 64 tokens x 128 ch, MN-major B
+constexpr uint32_t OP_A3 = 131072;     // [-W; Q . exp(G)], fp16, 128 rows x 128 ch, K-major A
+constexpr uint32_t OP_S = 163840;      // S0, fp16, 128 rows (k) x 128 (v), MN-major B
+constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 128 ch, MN-major A
+constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
+constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
+constexpr uint32_t SM_BETA = 229376;   // fp32 [64]
+constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [128]: exp(G_L)
+constexpr uint32_t SM_BAR = SM_GAM + 512;    // 3 mbarriers
+constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
+constexpr uint32_t SMEM_USED = SM_MISC + 64;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
+static_assert(SCR_R + 3 * 256 * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
+static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
+static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint64_t WAIT_NS = 2000000000ull;   // bounded waits: 2 s
+constexpr float FP16_LIMIT = 60000.f;         // operands of G3 / G4 must stay below this
+
+enum { FLAG_TIMEOUT = 1, FLAG_RANGE = 2 };
+
+struct Params {
+    CUtensorMap tq, tk, tg, tv;
+    int N, T_total, H, num_slots, lpt;
+    const __nv_bfloat16 *beta;
+    const int32_t *cu;
+    float *pool;
+    const int32_t *init_slot, *out_slot, *snap_slot;
+    __nv_bfloat16 *o;
+    float scale;
+    int32_t *err;
+    int32_t order[KDA_MAX_LPT_SEQS];
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = gtimer();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (gtimer() - t0 > WAIT_NS) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16, fp32 accumulate; fmt 1 = bf16, 0 = fp16
+// (A and B always share one format).
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn, int fmt) {
+    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)a_mn << 15) |
+           ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+#define KDA_TMEM_LD32(taddr, r)                                                                   \
+    asm volatile(                                                                                 \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"  \
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"        \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),            \
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),            \
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
+        : "r"(taddr))
+#define KDA_TMEM_LD16(taddr, r)                                                                   \
+    asm volatile(                                                                                 \
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"  \
+        "%14,%15}, [%16];"                                                                        \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+          "=r"(r[14]), "=r"(r[15])                                                                \
+        : "r"(taddr))
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of the 16-byte chunk holding columns col..col+7 (col % 8 == 0) of
+// row `row` in a tile of `rows` rows x 128 16-bit columns stored as two boxes of
+// 64 columns, each box rows x 128 B with the 128-byte swizzle (chunk index
+// XOR row % 8).  This is both the TMA SWIZZLE_128B layout of a 64-column box and
+// the canonical SW128 operand layout (K-major when columns are K, MN-major when
+// columns are M or N).
+__device__ __forceinline__ uint32_t chunk_off(int row, int col, int rows) {
+    return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ void store_bf16(uint8_t *base, uint32_t off, const float *v8) {
+    *reinterpret_cast<uint4 *>(base + off) =
+        make_uint4(pack_bf16x2(v8[0], v8[1]), pack_bf16x2(v8[2], v8[3]),
+                   pack_bf16x2(v8[4], v8[5]), pack_bf16x2(v8[6], v8[7]));
+}
+__device__ __forceinline__ void store_f16(uint8_t *base, uint32_t off, const float *v8) {
+    *reinterpret_cast<uint4 *>(base + off) =
+        make_uint4(pack_f16x2(v8[0], v8[1]), pack_f16x2(v8[2], v8[3]), pack_f16x2(v8[4], v8[5]),
+                   pack_f16x2(v8[6], v8[7]));
+}
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): two bf16 chunks.
+__device__ __forceinline__ void store_bf16_split(uint8_t *base, uint32_t off_hi, uint32_t off_lo,
+                                                 const float *v8) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = __bfloat162float(__float2bfloat16_rn(v8[i]));
+        lo[i] = v8[i] - hi[i];
+    }
+    store_bf16(base, off_hi, hi);
+    store_bf16(base, off_lo, lo);
+}
+__device__ __forceinline__ void unpack_bf16(const uint4 &w, float *v8) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v8[2 * i] = f.x;
+        v8[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ float absmax(const float *v, int n) {
+    float m = 0.f;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lq = warp & 3;     // TMEM lane quarter this warp may access
+    const int cq = warp >> 2;    // column quarter (0..3)
+    float *beta_s = reinterpret_cast<float *>(sm + SM_BETA);
+    float *gam_s = reinterpret_cast<float *>(sm + SM_GAM);
+    float *As = reinterpret_cast<float *>(sm + SCR_A);
+    float *Rs = reinterpret_cast<float *>(sm + SCR_R);
+    float *Ts = reinterpret_cast<float *>(sm + SCR_T);
+    const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
+                   bar_mma = sbase + SM_BAR + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM_MISC);
+    int *flags = reinterpret_cast<int *>(sm + SM_MISC + 4);
+
+    // ---- the unit: longest sequences first ------------------------------
+    const int ui = blockIdx.x / p.H, h = blockIdx.x - (blockIdx.x / p.H) * p.H;
+    const int n = p.lpt ? p.order[ui] : ui;
+    const int bos = p.cu[n], eos = p.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > p.T_total) {
+        if (tid == 0 && h == 0) report(p.err, DEVERR_SEQLENS);
+        return;
+    }
+    const int si = p.init_slot[n], so = p.out_slot[n];
+    const int ss = p.snap_slot ? p.snap_slot[n] : -1;
+    if (si < -1 || si >= p.num_slots || so < 0 || so >= p.num_slots || ss >= p.num_slots) {
+        if (tid == 0 && h == 0) report(p.err, DEVERR_SLOT_RANGE);
+        return;
+    }
+    const int nchunks = (eos - bos + C - 1) / C;
+
+    // ---- set-up -----------------------------------------------------------
+    if (tid == 0) {
+        mbar_init(bar_qkg, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_mma, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *flags = 0;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (tid == 0 && nchunks > 0) {
+        mbar_expect_tx(bar_qkg, 3 * 16384);
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sbase + RAW_Q + b * 8192, &p.tq, bar_qkg, 64 * b, h, bos);
+            tma_load_3d(sbase + RAW_K + b * 8192, &p.tk, bar_qkg, 64 * b, h, bos);
+            tma_load_3d(sbase + RAW_G + b * 8192, &p.tg, bar_qkg, 64 * b, h, bos);
+        }
+        mbar_expect_tx(bar_v, 16384);
+        for (int b = 0; b < 2; ++b)
+            tma_load_3d(sbase + RAW_V + b * 8192, &p.tv, bar_v, 64 * b, h, bos);
+    }
+
+    // ---- initial state: row k = 32*lq + lane, columns 32*cq .. 32*cq+31 ---
+    const int srow = 32 * lq + lane;
+    float S[32];
+    if (si >= 0) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.pool + ((size_t)si * p.H + h) * STATE_ELEMS + (size_t)srow * VD + 32 * cq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = __ldcs(src + j);
+            S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = 0.f;
+    }
+    if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) store_f16(sm + OP_S, chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
+
+    const float LOG2E = 1.4426950408889634f;
+    constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 1);
+    constexpr uint32_t ID_G2 = idesc(128, 128, 0, 1, 1);
+    constexpr uint32_t ID_G3 = idesc(128, 128, 0, 1, 0);
+    constexpr uint32_t ID_G4A = idesc(128, 128, 0, 1, 0);
+    constexpr uint32_t ID_G4B = idesc(128, 128, 1, 1, 0);
+    bool aborted = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = bos + c * C;
+        const int L = min(C, eos - t0);
+        const uint32_t par = (uint32_t)(c & 1);
+
+        // (1) raw q, k, gk have landed: take this thread's share into registers
+        if (!mbar_wait(bar_qkg, par)) atomicOr(flags, FLAG_TIMEOUT);
+        if (tid < C)
+            beta_s[tid] = (tid < L) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * p.H + h]) : 0.f;
+        // warp w owns key channels 8w .. 8w+7; lane l owns rows l and l + 32
+        const int ch = 8 * warp;
+        const int r0 = lane, r1 = lane + 32;
+        const uint4 wq0 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r0, ch, 64));
+        const uint4 wq1 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r1, ch, 64));
+        const uint4 wk0 = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(r0, ch, 64));
+        const uint4 wk1 = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(r1, ch, 64));
+        const uint4 wg0 = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(r0, ch, 64));
+        const uint4 wg1 = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(r1, ch, 64));
+        __syncthreads();   // R1 may now be overwritten
+        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+
+        // (2) cumulative decays and the operand tiles
+        {
+            float g0[8], g1[8];
+            unpack_bf16(wg0, g0);
+            unpack_bf16(wg1, g1);
+            const bool v0 = r0 < L, v1 = r1 < L;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (!v0) g0[i] = 0.f;
+                if (!v1) g1[i] = 0.f;
+            }
+            // inclusive prefix sums over rows 0..31 and 32..63
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float a = __shfl_up_sync(0xffffffffu, g0[i], off);
+                    const float b = __shfl_up_sync(0xffffffffu, g1[i], off);
+                    if (lane >= off) { g0[i] += a; g1[i] += b; }
+                }
+            }
+            float gref[8], glast[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                gref[i] = __shfl_sync(0xffffffffu, g0[i], 31);   // G at row 31
+                g1[i] += gref[i];
+                glast[i] = __shfl_sync(0xffffffffu, g1[i], 31);  // G at row 63 (= last valid row)
+            }
+            bool bad = false;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = half ? r1 : r0;
+                const bool valid = half ? v1 : v0;
+                const float *g = half ? g1 : g0;
+                float qq[8], kk[8];
+                unpack_bf16(half ? wq1 : wq0, qq);
+                unpack_bf16(half ? wk1 : wk0, kk);
+                float kf[8], kb[8], kt[8], ke[8], qr[8], qt[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float q_ = valid ? qq[i] : 0.f, k_ = valid ? kk[i] : 0.f;
+                    const float d = g[i] - gref[i];
+                    bad |= fabsf(d) > 85.f;
+                    const float ef = exp2f(d * LOG2E);           // exp(G_r - G_ref)
+                    const float eb = exp2f(-d * LOG2E);          // exp(G_ref - G_r)
+                    const float eg = exp2f(gref[i] * LOG2E) * ef;               // exp(G_r)
+                    const float el = exp2f((glast[i] - gref[i]) * LOG2E) * eb;  // exp(G_L - G_r)
+                    kf[i] = k_ * ef;
+                    kb[i] = k_ * eb;
+                    kt[i] = k_ * eg;
+                    ke[i] = k_ * el;
+                    qr[i] = q_ * ef;
+                    qt[i] = q_ * eg;
+                }
+                store_bf16_split(sm, OP_A1H + chunk_off(r, ch, 128), OP_A1L + chunk_off(r, ch, 128), kf);
+                store_bf16_split(sm, OP_A1H + chunk_off(64 + r, ch, 128),
+                                 OP_A1L + chunk_off(64 + r, ch, 128), qr);
+                store_bf16_split(sm, OP_B1H + chunk_off(r, ch, 64), OP_B1L + chunk_off(r, ch, 64), kb);
+                store_bf16(sm, OP_KT + chunk_off(r, ch, 64), kt);
+                store_f16(sm, OP_KE + chunk_off(r, ch, 64), ke);
+                store_f16(sm, OP_A3 + chunk_off(64 + r, ch, 128), qt);
+            }
+            if (bad) atomicOr(flags, FLAG_RANGE);
+            if (lane == 31) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) gam_s[ch + i] = expf(glast[i]);
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+
+        // (3) G1 as hi*hi + lo*hi + hi*lo
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                const uint32_t a0 = sbase + (t == 1 ? OP_A1L : OP_A1H);
+                const uint32_t b0 = sbase + (t == 2 ? OP_B1L : OP_B1H);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma(tmem, sdesc(a0 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                        sdesc(b0 + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), ID_G1, (t | s) != 0);
+            }
+            mma_commit(bar_mma);
+        }
+
+        // (4) A -> fp32 scratch (strictly lower, x beta_r); Aqk -> fp16 rows
+        //     128..191 of TBZ (lower incl. diagonal); then prefetch the next
+        //     chunk's q, k, gk into R1 (G1 has consumed it)
+        if (!mbar_wait(bar_mma, 0)) atomicOr(flags, FLAG_TIMEOUT);
+        tc_fence_after();
+        if (tid == 0 && c + 1 < nchunks) {
+            mbar_expect_tx(bar_qkg, 3 * 16384);
+            for (int b = 0; b < 2; ++b) {
+                tma_load_3d(sbase + RAW_Q + b * 8192, &p.tq, bar_qkg, 64 * b, h, t0 + C);
+                tma_load_3d(sbase + RAW_K + b * 8192, &p.tk, bar_qkg, 64 * b, h, t0 + C);
+                tma_load_3d(sbase + RAW_G + b * 8192, &p.tg, bar_qkg, 64 * b, h, t0 + C);
+            }
+        }
+        {
+            uint32_t r[16];
+            KDA_TMEM_LD16(tmem + ((uint32_t)(32 * lq) << 16) + 16 * cq, r);
+            tmem_wait_ld();
+            const int row = 32 * (lq & 1) + lane;   // 0..63 within A or Aqk
+            float v[16];
+            if (lq < 2) {
+                const float b = beta_s[row];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    v[j] = (16 * cq + j < row) ? __uint_as_float(r[j]) * b : 0.f;
+                float4 *dst = reinterpret_cast<float4 *>(As + row * AS + 16 * cq);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = (16 * cq + j <= row) ? __uint_as_float(r[j]) : 0.f;
+                store_f16(sm, OP_TBZ + (uint32_t)(128 + row) * 128 + ((((2 * cq) ^ row) & 7) << 4), v);
+                store_f16(sm, OP_TBZ + (uint32_t)(128 + row) * 128 + ((((2 * cq + 1) ^ row) & 7) << 4),
+                          v + 8);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // (5) T = (I + A)^-1, 16 x 16 blocks.  Diagonal blocks by forward
+        //     substitution (warp I, lane = column), then block diagonals d = 1..3:
+        //     T_IJ = -T_II (sum_{K=J}^{I-1} A_IK T_KJ).
+        if (warp < 4 && lane < 16) {
+            const int I = warp, col = lane;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < r; ++j) acc = fmaf(As[(16 * I + r) * AS + 16 * I + j], x[j], acc);
+                if (r > col) x[r] = -acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * 64 + 16 * I + col] = x[r];
+        }
+        __syncthreads();
+        for (int d = 1; d < 4; ++d) {
+            const int nb = 4 - d;
+            for (int e = tid; e < nb * 256; e += NT) {
+                const int b = e >> 8, I = d + b, J = b, r = (e >> 4) & 15, col = e & 15;
+                const float *arow = As + (16 * I + r) * AS;
+                float acc = 0.f;
+                for (int m = 16 * J; m < 16 * I; ++m) acc = fmaf(arow[m], Ts[m * 64 + 16 * J + col], acc);
+                Rs[e] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < nb * 256; e += NT) {
+                const int b = e >> 8, I = d + b, J = b, r = (e >> 4) & 15, col = e & 15;
+                const float *trow = Ts + (16 * I + r) * 64 + 16 * I;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc = fmaf(trow[m], Rs[(b << 8) + m * 16 + col], acc);
+                Ts[(16 * I + r) * 64 + 16 * J + col] = -acc;
+            }
+            __syncthreads();
+        }
+        // T Diag(beta) -> bf16 rows 0..63 of TBZ; rows 64..127 zero
+        {
+            const int r = tid >> 3, cc = tid & 7;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int col = 8 * cc + j;
+                v[j] = ((col >> 4) <= (r >> 4)) ? Ts[r * 64 + col] * beta_s[col] : 0.f;
+            }
+            store_bf16(sm, OP_TBZ + (uint32_t)r * 128 + (((cc ^ r) & 7) << 4), v);
+            *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * tid) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncthreads();
+
+        // (6) G2: [T Diag(b); 0] x [K~ | V]
+        if (tid == 0) {
+            if (!mbar_wait(bar_v, par)) atomicOr(flags, FLAG_TIMEOUT);
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t a = sdesc(sbase + OP_TBZ + s * 32, 16, 1024);
+                mma(tmem, a, sdesc(sbase + OP_KT + s * 2048, 8192, 1024), ID_G2, s > 0);
+                mma(tmem + 128, a, sdesc(sbase + RAW_V + s * 2048, 8192, 1024), ID_G2, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, 1)) atomicOr(flags, FLAG_TIMEOUT);
+        tc_fence_after();
+        // (7) -W -> fp16 rows 0..63 of [-W; Q~]; prefetch the next v (G2 consumed it)
+        if (tid == 0 && c + 1 < nchunks) {
+            mbar_expect_tx(bar_v, 16384);
+            for (int b = 0; b < 2; ++b)
+                tma_load_3d(sbase + RAW_V + b * 8192, &p.tv, bar_v, 64 * b, h, t0 + C);
+        }
+        if (lq < 2) {
+            uint32_t r[32];
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
+            tmem_wait_ld();
+            const int row = 32 * lq + lane;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = -__uint_as_float(r[j]);
+            if (absmax(v, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                store_f16(sm, OP_A3 + chunk_off(row, 32 * cq + 8 * j, 128), v + 8 * j);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+
+        // (8) G3: [-W; Q~] x S0 accumulated onto [U~; 0]
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma(tmem + 128, sdesc(sbase + OP_A3 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                    sdesc(sbase + OP_S + s * 2048, 16384, 1024), ID_G3, 1);
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, 0)) atomicOr(flags, FLAG_TIMEOUT);
+        tc_fence_after();
+        // (9) U -> fp16 MN-major [token][v]
+        if (lq < 2) {
+            uint32_t r[32];
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+            tmem_wait_ld();
+            const int row = 32 * lq + lane;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            if (absmax(v, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                store_f16(sm, OP_U + chunk_off(row, 32 * cq + 8 * j, 64), v + 8 * j);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+
+        // (10) G4a: [0; Aqk] x U onto cols 128..; G4b: K_end^T x U into cols 0..127
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t b = sdesc(sbase + OP_U + s * 2048, 8192, 1024);
+                mma(tmem + 128, sdesc(sbase + OP_TBZ + 8192 + s * 32, 16, 1024), b, ID_G4A, 1);
+                mma(tmem, sdesc(sbase + OP_KE + s * 2048, 8192, 1024), b, ID_G4B, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        if (!mbar_wait(bar_mma, 1)) atomicOr(flags, FLAG_TIMEOUT);
+        tc_fence_after();
+        // (11) outputs (rows 64..127 of cols 128..255) and the state update
+        if (lq >= 2) {
+            uint32_t r[32];
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+            tmem_wait_ld();
+            const int row = 32 * (lq - 2) + lane;
+            if (row < L) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + row) * p.H + h) * VD + 32 * cq);
+                const float sc = p.scale;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float *f = reinterpret_cast<const float *>(r + 8 * j);
+                    dst[j] = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
+                                        pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
+                }
+            }
+        }
+        {
+            uint32_t r[32];
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
+            tmem_wait_ld();
+            const float gm = gam_s[srow];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[j] = fmaf(gm, S[j], __uint_as_float(r[j]));
+            if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                store_f16(sm, OP_S + chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+    }
+
+    if ((*flags & FLAG_RANGE) && tid == 0) report(p.err, DEVERR_RANGE);
+    if (aborted) {
+        if (tid == 0) report(p.err, DEVERR_TIMEOUT);
+    } else {
+        float4 *dst = reinterpret_cast<float4 *>(p.pool + ((size_t)so * p.H + h) * STATE_ELEMS +
+                                                 (size_t)srow * VD + 32 * cq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            __stcs(dst + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
+        if (ss >= 0) {
+            float4 *d2 = reinterpret_cast<float4 *>(p.pool + ((size_t)ss * p.H + h) * STATE_ELEMS +
+                                                    (size_t)srow * VD + 32 * cq);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                __stcs(d2 + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS));
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [T][H][128] bf16 viewed as a 3-D tensor {128, H, T}; boxes of 64 channels x 1 head x 64 tokens.
+bool make_map(CUtensorMap *m, const void *base, int H, int T) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
+    using namespace tc;
+    Params p;   // ~9 KB, copied into the launch parameters
+    memset(&p, 0, sizeof(p));
+    if (a.T_total > 0) {
+        if (!make_map(&p.tq, a.q, a.H, a.T_total) || !make_map(&p.tk, a.k, a.H, a.T_total) ||
+            !make_map(&p.tg, a.gk, a.H, a.T_total) || !make_map(&p.tv, a.v, a.H, a.T_total))
+            return cudaErrorInvalidValue;
+    }
+    p.N = a.N; p.T_total = a.T_total; p.H = a.H; p.num_slots = a.num_slots;
+    p.beta = (const __nv_bfloat16 *)a.beta; p.cu = a.cu; p.pool = a.pool;
+    p.init_slot = a.init_slot; p.out_slot = a.out_slot; p.snap_slot = a.snap_slot;
+    p.o = (__nv_bfloat16 *)a.o; p.scale = a.scale; p.err = a.err;
+    p.lpt = a.N <= KDA_MAX_LPT_SEQS;
+    if (p.lpt) {
+        std::vector<int> idx(a.N);
+        std::iota(idx.begin(), idx.end(), 0);
+        std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
+            return a.cu_host[x + 1] - a.cu_host[x] > a.cu_host[y + 1] - a.cu_host[y];
+        });
+        for (int i = 0; i < a.N; ++i) p.order[i] = idx[i];
+    }
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    prefill_tc_kernel<<<(unsigned)(a.N * a.H), NT, SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
