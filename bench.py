@@ -161,14 +161,7 @@ def timed(fn, steps, warmup, ws, sampler=None, stream=None):
 # ---------------------------------------------------------------------------
 
 def varlen_workload(device, seed=1, H=64):
-    g = gen.make_gen(seed)
-    lengths = gen.varlen_lengths(8, 64, 2048, g)
-    cu = gen.cu_seqlens(lengths)
-    T = int(cu[-1])
-    gd = gen.make_gen(seed + 1000, device)
-    x = gen.token_inputs(T, H, torch.bfloat16, gd, device=device)
-    ck = gen.checkpoint((8, H, KD, VD), gd, device=device)
-    return dict(lengths=lengths, cu=cu, T=T, H=H, x=x, ck=ck, N=8)
+    return gen.varlen_batch(device, seed=seed, H=H)
 
 
 def algorithmic_prefill_bytes(T, H, N, es=2, init_read=True, snap=False):
@@ -408,10 +401,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the decode / verify+fold runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--only", choices=["decode", "verify"], default=None,
+                    help="run one of the secondary workloads alone (for profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.only:
+        torch.cuda.set_device(local)
+        from kda_state_gb300 import _build
+        _build.build()
+        fn = bench_decode if args.only == "decode" else bench_verify_fold
+        r = fn(args, 1, steps=args.steps)
+        print(json.dumps({"only": args.only, **{k: v for k, v in r.items()
+                                                 if isinstance(v, (int, float))}}), flush=True)
         return
     if ws > 1:
         torch.cuda.set_device(local)

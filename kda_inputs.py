@@ -97,3 +97,27 @@ WORKLOADS = {
     "verify": dict(B=64, G=8, H=64, slots=128, layers=69, ring=16, accept_p=0.64, dtype="bf16",
                    seed=4),
 }
+
+
+# ---------------------------------------------------------------------------
+# Full workload batches (same recipe for the benchmark and the parity tests).
+# Large tensors are drawn on `device` with a generator seeded seed + 1000.
+# ---------------------------------------------------------------------------
+
+def varlen_batch(device: str = "cpu", seed: int = 1, H: int = 64, N: int = 8, lo: int = 64,
+                 hi: int = 2048, dtype=torch.bfloat16):
+    g = make_gen(seed)
+    lengths = varlen_lengths(N, lo, hi, g)
+    cu = cu_seqlens(lengths)
+    gd = make_gen(seed + 1000, device)
+    x = token_inputs(int(cu[-1]), H, dtype, gd, device=device)
+    ck = checkpoint((N, H, K_DIM, V_DIM), gd, device=device)
+    return dict(lengths=lengths, cu=cu, T=int(cu[-1]), H=H, N=N, x=x, ck=ck)
+
+
+def long_batch(device: str = "cpu", seed: int = 2, H: int = 96, N: int = 4, T: int = 24576,
+               dtype=torch.bfloat16):
+    gd = make_gen(seed + 1000, device)
+    x = token_inputs(N * T, H, dtype, gd, device=device)
+    ck = checkpoint((N, H, K_DIM, V_DIM), gd, device=device)
+    return dict(N=N, T=T, H=H, x=x, ck=ck)

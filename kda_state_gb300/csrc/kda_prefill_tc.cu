@@ -73,7 +73,6 @@ constexpr uint32_t RAW_Q = 0;          // 64 tokens x 128 ch bf16, 2 boxes of 64
 constexpr uint32_t RAW_K = 16384;
 constexpr uint32_t RAW_G = 32768;
 constexpr uint32_t SCR_A = 49152;      // fp32 A [64][AS]
-constexpr uint32_t SCR_R = SCR_A + 64 * AS * 4;   // fp32 block products, 3 x 256
 constexpr uint32_t OP_TBZ = 69632;     // rows 0-63 T Diag(b) (bf16), 64-127 zero, 128-191 Aqk (fp16)
 constexpr uint32_t R1_END = 98304;
 constexpr uint32_t RAW_V = 98304;      // v, bf16, also the MN-major B operand of U~ = T Diag(b) V
@@ -89,7 +88,9 @@ constexpr uint32_t SM_BAR = SM_GAM + 512;    // 3 mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
-static_assert(SCR_R + 3 * 256 * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
+static_assert(SCR_A + 64 * AS * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
+static_assert(6 * 16 * 20 * 4 <= 8192, "M blocks overflow TBZ rows 0-63");
+static_assert(4 * 16 * 17 * 4 <= 8192, "transposed diagonal blocks overflow TBZ rows 64-127");
 static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 
@@ -143,6 +144,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (ok) return true;
         if (gtimer() - t0 > WAIT_NS) return false;
     }
+}
+// Completion of this CTA's MMAs: thread 0 waits (bounded) on the commit
+// barrier, the block synchronises, every thread fences before reading TMEM.
+__device__ __forceinline__ void mma_wait_all(uint32_t bar, uint32_t parity, int *flags) {
+    if (threadIdx.x == 0 && !mbar_wait(bar, parity)) atomicOr(flags, 1);
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int c0, int c1, int c2) {
@@ -253,10 +261,67 @@ __device__ __forceinline__ void unpack_bf16(const uint4 &w, float *v8) {
         v8[2 * i + 1] = f.y;
     }
 }
+// 2^x on the special-function unit (one MUFU op; relative error ~2^-22, far
+// below the bf16/fp16 rounding of the operands it feeds).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float absmax(const float *v, int n) {
     float m = 0.f;
     for (int i = 0; i < n; ++i) m = fmaxf(m, fabsf(v[i]));
     return m;
+}
+
+// ---------------------------------------------------------------------------
+// 64 x 64 unit-lower-triangular inverse helpers (fp32, shared memory).
+// A is [64][AS] (strictly lower), T is [64][64], M holds the six blocks
+// M_IK = T_II A_IK (I > K) at index I(I-1)/2 + K, 16 rows of MS floats each.
+// Each thread produces one row of 4 consecutive columns of a 16 x 16 block.
+// ---------------------------------------------------------------------------
+constexpr int MS = 20;   // row stride (floats) of an M block: spreads rows over banks
+// TdT holds the diagonal blocks transposed, TdT[(I*16 + m)*17 + r] = T_II[r][m].
+__device__ __forceinline__ void solve_m_stage(const float *As, const float *TdT, float *Ms, int tid) {
+    if (tid >= 6 * 64) return;
+    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    const int I = (b == 0) ? 1 : (b < 3 ? 2 : 3);
+    const int K = b - I * (I - 1) / 2;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float t = TdT[(I * 16 + m) * 17 + r];
+        const float4 a = *reinterpret_cast<const float4 *>(As + (16 * I + m) * AS + 16 * K + c4);
+        acc.x = fmaf(t, a.x, acc.x);
+        acc.y = fmaf(t, a.y, acc.y);
+        acc.z = fmaf(t, a.z, acc.z);
+        acc.w = fmaf(t, a.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Ms + (b * 16 + r) * MS + c4) = acc;
+}
+
+template <int D>
+__device__ __forceinline__ void solve_level(const float *Ms, float *Ts, int tid) {
+    constexpr int NB = 4 - D;   // blocks (J + D, J), J = 0 .. NB-1
+    if (tid >= NB * 64) return;
+    const int J = tid >> 6, I = J + D, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < D; ++kk) {
+        const int K = J + kk;
+        const float *mrow = Ms + ((I * (I - 1) / 2 + K) * 16 + r) * MS;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float mv = mrow[m];
+            const float4 t = *reinterpret_cast<const float4 *>(Ts + (16 * K + m) * 64 + 16 * J + c4);
+            acc.x = fmaf(mv, t.x, acc.x);
+            acc.y = fmaf(mv, t.y, acc.y);
+            acc.z = fmaf(mv, t.z, acc.z);
+            acc.w = fmaf(mv, t.w, acc.w);
+        }
+    }
+    *reinterpret_cast<float4 *>(Ts + (16 * I + r) * 64 + 16 * J + c4) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
 }
 
 // ---------------------------------------------------------------------------
@@ -272,7 +337,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *beta_s = reinterpret_cast<float *>(sm + SM_BETA);
     float *gam_s = reinterpret_cast<float *>(sm + SM_GAM);
     float *As = reinterpret_cast<float *>(sm + SCR_A);
-    float *Rs = reinterpret_cast<float *>(sm + SCR_R);
+    float *Ms = reinterpret_cast<float *>(sm + OP_TBZ);          // solve scratch until TB is written
+    float *TdT = reinterpret_cast<float *>(sm + OP_TBZ + 8192);  // likewise (TBZ rows 64..127)
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
                    bar_mma = sbase + SM_BAR + 16;
@@ -346,6 +412,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     for (int j = 0; j < 4; ++j) store_f16(sm + OP_S, chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
 
     const float LOG2E = 1.4426950408889634f;
+    // beta of the chunk about to be processed, loaded one chunk ahead
+    float beta_next = 0.f;
+    if (tid < C && nchunks > 0 && tid < min(C, eos - bos))
+        beta_next = __bfloat162float(p.beta[(size_t)(bos + tid) * p.H + h]);
     constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 1);
     constexpr uint32_t ID_G2 = idesc(128, 128, 0, 1, 1);
     constexpr uint32_t ID_G3 = idesc(128, 128, 0, 1, 0);
@@ -359,8 +429,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 
         // (1) raw q, k, gk have landed: take this thread's share into registers
         if (!mbar_wait(bar_qkg, par)) atomicOr(flags, FLAG_TIMEOUT);
-        if (tid < C)
-            beta_s[tid] = (tid < L) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * p.H + h]) : 0.f;
+        if (tid < C) {
+            beta_s[tid] = beta_next;
+            const int tn = t0 + C + tid;
+            beta_next = (c + 1 < nchunks && tn < eos) ? __bfloat162float(p.beta[(size_t)tn * p.H + h]) : 0.f;
+        }
         // warp w owns key channels 8w .. 8w+7; lane l owns rows l and l + 32
         const int ch = 8 * warp;
         const int r0 = lane, r1 = lane + 32;
@@ -402,6 +475,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 glast[i] = __shfl_sync(0xffffffffu, g1[i], 31);  // G at row 63 (= last valid row)
             }
             bool bad = false;
+            float egr[8], elr[8];   // per channel: exp(G_ref), exp(G_L - G_ref)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                egr[i] = ex2(gref[i] * LOG2E);
+                elr[i] = ex2((glast[i] - gref[i]) * LOG2E);
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int r = half ? r1 : r0;
@@ -414,18 +493,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float q_ = valid ? qq[i] : 0.f, k_ = valid ? kk[i] : 0.f;
-                    const float d = g[i] - gref[i];
-                    bad |= fabsf(d) > 85.f;
-                    const float ef = exp2f(d * LOG2E);           // exp(G_r - G_ref)
-                    const float eb = exp2f(-d * LOG2E);          // exp(G_ref - G_r)
-                    const float eg = exp2f(gref[i] * LOG2E) * ef;               // exp(G_r)
-                    const float el = exp2f((glast[i] - gref[i]) * LOG2E) * eb;  // exp(G_L - G_r)
+                    const float d = (g[i] - gref[i]) * LOG2E;
+                    bad |= fabsf(d) > 85.f * LOG2E;
+                    const float ef = ex2(d);                 // exp(G_r - G_ref)
+                    const float eb = ex2(-d);                // exp(G_ref - G_r)
                     kf[i] = k_ * ef;
                     kb[i] = k_ * eb;
-                    kt[i] = k_ * eg;
-                    ke[i] = k_ * el;
+                    kt[i] = k_ * (egr[i] * ef);              // k exp(G_r)
+                    ke[i] = k_ * (elr[i] * eb);              // k exp(G_L - G_r)
                     qr[i] = q_ * ef;
-                    qt[i] = q_ * eg;
+                    qt[i] = q_ * (egr[i] * ef);              // q exp(G_r)
                 }
                 store_bf16_split(sm, OP_A1H + chunk_off(r, ch, 128), OP_A1L + chunk_off(r, ch, 128), kf);
                 store_bf16_split(sm, OP_A1H + chunk_off(64 + r, ch, 128),
@@ -462,8 +539,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         // (4) A -> fp32 scratch (strictly lower, x beta_r); Aqk -> fp16 rows
         //     128..191 of TBZ (lower incl. diagonal); then prefetch the next
         //     chunk's q, k, gk into R1 (G1 has consumed it)
-        if (!mbar_wait(bar_mma, 0)) atomicOr(flags, FLAG_TIMEOUT);
-        tc_fence_after();
+        mma_wait_all(bar_mma, 0, flags);
         if (tid == 0 && c + 1 < nchunks) {
             mbar_expect_tx(bar_qkg, 3 * 16384);
             for (int b = 0; b < 2; ++b) {
@@ -498,9 +574,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
 
-        // (5) T = (I + A)^-1, 16 x 16 blocks.  Diagonal blocks by forward
-        //     substitution (warp I, lane = column), then block diagonals d = 1..3:
-        //     T_IJ = -T_II (sum_{K=J}^{I-1} A_IK T_KJ).
+        // (5) T = (I + A)^-1 in 16 x 16 blocks.  S1: diagonal blocks T_II by
+        //     forward substitution (warp I, lane = column).  M: M_IK = T_II A_IK
+        //     for I > K.  Levels d = 1..3: T_IJ = -sum_{K=J}^{I-1} M_IK T_KJ with
+        //     I - J = d (every term is from a lower level).
         if (warp < 4 && lane < 16) {
             const int I = warp, col = lane;
             float x[16];
@@ -508,35 +585,29 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
 #pragma unroll
             for (int r = 1; r < 16; ++r) {
-                float acc = 0.f;
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < r; ++j) acc = fmaf(As[(16 * I + r) * AS + 16 * I + j], x[j], acc);
-                if (r > col) x[r] = -acc;
+                for (int j = 0; j < r; ++j) {
+                    const float a = As[(16 * I + r) * AS + 16 * I + j] * x[j];
+                    if (j & 1) a1 += a; else a0 += a;
+                }
+                if (r > col) x[r] = -(a0 + a1);
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * 64 + 16 * I + col] = x[r];
+            for (int r = 0; r < 16; ++r) {
+                Ts[(16 * I + r) * 64 + 16 * I + col] = x[r];
+                TdT[(I * 16 + col) * 17 + r] = x[r];   // TdT[I][m][r] = T_II[r][m]
+            }
         }
         __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            const int nb = 4 - d;
-            for (int e = tid; e < nb * 256; e += NT) {
-                const int b = e >> 8, I = d + b, J = b, r = (e >> 4) & 15, col = e & 15;
-                const float *arow = As + (16 * I + r) * AS;
-                float acc = 0.f;
-                for (int m = 16 * J; m < 16 * I; ++m) acc = fmaf(arow[m], Ts[m * 64 + 16 * J + col], acc);
-                Rs[e] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += NT) {
-                const int b = e >> 8, I = d + b, J = b, r = (e >> 4) & 15, col = e & 15;
-                const float *trow = Ts + (16 * I + r) * 64 + 16 * I;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc = fmaf(trow[m], Rs[(b << 8) + m * 16 + col], acc);
-                Ts[(16 * I + r) * 64 + 16 * J + col] = -acc;
-            }
-            __syncthreads();
-        }
+        solve_m_stage(As, TdT, Ms, tid);
+        __syncthreads();
+        solve_level<1>(Ms, Ts, tid);
+        __syncthreads();
+        solve_level<2>(Ms, Ts, tid);
+        __syncthreads();
+        solve_level<3>(Ms, Ts, tid);
+        __syncthreads();
         // T Diag(beta) -> bf16 rows 0..63 of TBZ; rows 64..127 zero
         {
             const int r = tid >> 3, cc = tid & 7;
@@ -564,8 +635,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             }
             mma_commit(bar_mma);
         }
-        if (!mbar_wait(bar_mma, 1)) atomicOr(flags, FLAG_TIMEOUT);
-        tc_fence_after();
+        mma_wait_all(bar_mma, 1, flags);
         // (7) -W -> fp16 rows 0..63 of [-W; Q~]; prefetch the next v (G2 consumed it)
         if (tid == 0 && c + 1 < nchunks) {
             mbar_expect_tx(bar_v, 16384);
@@ -599,8 +669,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                     sdesc(sbase + OP_S + s * 2048, 16384, 1024), ID_G3, 1);
             mma_commit(bar_mma);
         }
-        if (!mbar_wait(bar_mma, 0)) atomicOr(flags, FLAG_TIMEOUT);
-        tc_fence_after();
+        mma_wait_all(bar_mma, 0, flags);
         // (9) U -> fp16 MN-major [token][v]
         if (lq < 2) {
             uint32_t r[32];
@@ -630,8 +699,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             }
             mma_commit(bar_mma);
         }
-        if (!mbar_wait(bar_mma, 1)) atomicOr(flags, FLAG_TIMEOUT);
-        tc_fence_after();
+        mma_wait_all(bar_mma, 1, flags);
         // (11) outputs (rows 64..127 of cols 128..255) and the state update
         if (lq >= 2) {
             uint32_t r[32];
