@@ -89,8 +89,7 @@ constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 static_assert(SCR_A + 64 * AS * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
-static_assert(6 * 16 * 20 * 4 <= 8192, "M blocks overflow TBZ rows 0-63");
-static_assert(4 * 16 * 17 * 4 <= 8192, "transposed diagonal blocks overflow TBZ rows 64-127");
+static_assert(3 * 16 * 24 * 4 <= 8192, "R scratch overflows TBZ rows 0-63");
 static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 
@@ -275,53 +274,85 @@ __device__ __forceinline__ float absmax(const float *v, int n) {
 }
 
 // ---------------------------------------------------------------------------
-// 64 x 64 unit-lower-triangular inverse helpers (fp32, shared memory).
-// A is [64][AS] (strictly lower), T is [64][64], M holds the six blocks
-// M_IK = T_II A_IK (I > K) at index I(I-1)/2 + K, 16 rows of MS floats each.
-// Each thread produces one row of 4 consecutive columns of a 16 x 16 block.
+// 64 x 64 unit-lower-triangular inverse, off-diagonal blocks.
+// A is fp32 [64][AS] (strictly lower, rows scaled by beta); T is fp32 [64][64]
+// with its columns XOR-swizzled by row: T[r][c] lives at r*64 + tsw(r, c).
+// Warp J owns block column J: for I = J+1 .. 3 it forms
+//     R = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II R
+// from blocks of lower levels only, so the warps need no block-wide barrier.
+// The 16 x 16 x 16 products run as warp-level m16n8k8 TF32 MMAs (fp32
+// accumulate): they are latency-bound and far below the 64-row minimum of the
+// 5th-generation MMA; T is rounded to bf16 right after.
 // ---------------------------------------------------------------------------
-constexpr int MS = 20;   // row stride (floats) of an M block: spreads rows over banks
-// TdT holds the diagonal blocks transposed, TdT[(I*16 + m)*17 + r] = T_II[r][m].
-__device__ __forceinline__ void solve_m_stage(const float *As, const float *TdT, float *Ms, int tid) {
-    if (tid >= 6 * 64) return;
-    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-    const int I = (b == 0) ? 1 : (b < 3 ? 2 : 3);
-    const int K = b - I * (I - 1) / 2;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float t = TdT[(I * 16 + m) * 17 + r];
-        const float4 a = *reinterpret_cast<const float4 *>(As + (16 * I + m) * AS + 16 * K + c4);
-        acc.x = fmaf(t, a.x, acc.x);
-        acc.y = fmaf(t, a.y, acc.y);
-        acc.z = fmaf(t, a.z, acc.z);
-        acc.w = fmaf(t, a.w, acc.w);
-    }
-    *reinterpret_cast<float4 *>(Ms + (b * 16 + r) * MS + c4) = acc;
+__device__ __forceinline__ int tsw(int r, int c) { return c ^ ((r & 3) << 3); }
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+        " {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+constexpr int RW = 24;   // row stride (floats) of a warp's 16 x 16 R scratch
 
-template <int D>
-__device__ __forceinline__ void solve_level(const float *Ms, float *Ts, int tid) {
-    constexpr int NB = 4 - D;   // blocks (J + D, J), J = 0 .. NB-1
-    if (tid >= NB * 64) return;
-    const int J = tid >> 6, I = J + D, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+template <int J>
+__device__ __forceinline__ void solve_block_column(const float *As, float *Ts, float *Rw, int lane) {
+    const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int kk = 0; kk < D; ++kk) {
-        const int K = J + kk;
-        const float *mrow = Ms + ((I * (I - 1) / 2 + K) * 16 + r) * MS;
+    for (int I = J + 1; I < 4; ++I) {
+        float rc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float mv = mrow[m];
-            const float4 t = *reinterpret_cast<const float4 *>(Ts + (16 * K + m) * 64 + 16 * J + c4);
-            acc.x = fmaf(mv, t.x, acc.x);
-            acc.y = fmaf(mv, t.y, acc.y);
-            acc.z = fmaf(mv, t.z, acc.z);
-            acc.w = fmaf(mv, t.w, acc.w);
+        for (int K = J; K < I; ++K) {
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const float *ar = As + (16 * I + g) * AS + 16 * K + 8 * ks + t4;
+                const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * AS]), to_tf32(ar[4]),
+                                       to_tf32(ar[8 * AS + 4])};
+                const int rr = 16 * K + 8 * ks + t4;   // rr % 4 == t4, also for rr + 4
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int cc = (16 * J + 8 * nt + g) ^ (t4 << 3);
+                    const uint32_t b[2] = {to_tf32(Ts[rr * 64 + cc]), to_tf32(Ts[(rr + 4) * 64 + cc])};
+                    mma_tf32(rc[nt], a, b);
+                }
+            }
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            Rw[g * RW + 8 * nt + 2 * t4] = rc[nt][0];
+            Rw[g * RW + 8 * nt + 2 * t4 + 1] = rc[nt][1];
+            Rw[(g + 8) * RW + 8 * nt + 2 * t4] = rc[nt][2];
+            Rw[(g + 8) * RW + 8 * nt + 2 * t4 + 1] = rc[nt][3];
+        }
+        __syncwarp();
+        float tc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int sw = (g & 3) << 3;   // swizzle of rows 16I + g and 16I + g + 8
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int c0 = (16 * I + 8 * ks + t4) ^ sw, c1 = (16 * I + 8 * ks + t4 + 4) ^ sw;
+            const uint32_t a[4] = {to_tf32(Ts[(16 * I + g) * 64 + c0]), to_tf32(Ts[(16 * I + g + 8) * 64 + c0]),
+                                   to_tf32(Ts[(16 * I + g) * 64 + c1]), to_tf32(Ts[(16 * I + g + 8) * 64 + c1])};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t b[2] = {to_tf32(Rw[(8 * ks + t4) * RW + 8 * nt + g]),
+                                       to_tf32(Rw[(8 * ks + t4 + 4) * RW + 8 * nt + g])};
+                mma_tf32(tc[nt], a, b);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = (16 * J + 8 * nt + 2 * t4) ^ sw;
+            Ts[(16 * I + g) * 64 + c] = -tc[nt][0];
+            Ts[(16 * I + g) * 64 + c + 1] = -tc[nt][1];
+            Ts[(16 * I + g + 8) * 64 + c] = -tc[nt][2];
+            Ts[(16 * I + g + 8) * 64 + c + 1] = -tc[nt][3];
+        }
+        __syncwarp();
     }
-    *reinterpret_cast<float4 *>(Ts + (16 * I + r) * 64 + 16 * J + c4) =
-        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
 }
 
 // ---------------------------------------------------------------------------
@@ -337,8 +368,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *beta_s = reinterpret_cast<float *>(sm + SM_BETA);
     float *gam_s = reinterpret_cast<float *>(sm + SM_GAM);
     float *As = reinterpret_cast<float *>(sm + SCR_A);
-    float *Ms = reinterpret_cast<float *>(sm + OP_TBZ);          // solve scratch until TB is written
-    float *TdT = reinterpret_cast<float *>(sm + OP_TBZ + 8192);  // likewise (TBZ rows 64..127)
+    float *Rws = reinterpret_cast<float *>(sm + OP_TBZ);   // per-warp R scratch until TB is written
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
                    bar_mma = sbase + SM_BAR + 16;
@@ -574,10 +604,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
 
-        // (5) T = (I + A)^-1 in 16 x 16 blocks.  S1: diagonal blocks T_II by
-        //     forward substitution (warp I, lane = column).  M: M_IK = T_II A_IK
-        //     for I > K.  Levels d = 1..3: T_IJ = -sum_{K=J}^{I-1} M_IK T_KJ with
-        //     I - J = d (every term is from a lower level).
+        // (5) T = (I + A)^-1 in 16 x 16 blocks: diagonal blocks T_II by forward
+        //     substitution (warp I, lane = column), then each warp completes its
+        //     block column (solve_block_column).
         if (warp < 4 && lane < 16) {
             const int I = warp, col = lane;
             float x[16];
@@ -594,19 +623,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 if (r > col) x[r] = -(a0 + a1);
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                Ts[(16 * I + r) * 64 + 16 * I + col] = x[r];
-                TdT[(I * 16 + col) * 17 + r] = x[r];   // TdT[I][m][r] = T_II[r][m]
-            }
+            for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * 64 + tsw(r, 16 * I + col)] = x[r];
         }
         __syncthreads();
-        solve_m_stage(As, TdT, Ms, tid);
-        __syncthreads();
-        solve_level<1>(Ms, Ts, tid);
-        __syncthreads();
-        solve_level<2>(Ms, Ts, tid);
-        __syncthreads();
-        solve_level<3>(Ms, Ts, tid);
+        if (warp == 0) solve_block_column<0>(As, Ts, Rws, lane);
+        else if (warp == 1) solve_block_column<1>(As, Ts, Rws + 16 * RW, lane);
+        else if (warp == 2) solve_block_column<2>(As, Ts, Rws + 32 * RW, lane);
         __syncthreads();
         // T Diag(beta) -> bf16 rows 0..63 of TBZ; rows 64..127 zero
         {
@@ -615,7 +637,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int col = 8 * cc + j;
-                v[j] = ((col >> 4) <= (r >> 4)) ? Ts[r * 64 + col] * beta_s[col] : 0.f;
+                v[j] = ((col >> 4) <= (r >> 4)) ? Ts[r * 64 + tsw(r, col)] * beta_s[col] : 0.f;
             }
             store_bf16(sm, OP_TBZ + (uint32_t)r * 128 + (((cc ^ r) & 7) << 4), v);
             *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * tid) = make_uint4(0, 0, 0, 0);
