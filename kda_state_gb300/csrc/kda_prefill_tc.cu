@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             const int tn = t0 + C + tid;
             beta_next = (c + 1 < nchunks && tn < eos) ? __bfloat162float(p.beta[(size_t)tn * p.H + h]) : 0.f;
         }
-        // warp w owns key channels 8w .. 8w+7; lane l owns rows l and l + 32
+        // warp w owns key channels 8w .. 8w+7; lane l owns rows 2l and 2l + 1
         const int ch = 8 * warp;
-        const int r0 = lane, r1 = lane + 32;
+        const int r0 = 2 * lane, r1 = 2 * lane + 1;
         const uint4 wq0 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r0, ch, 64));
         const uint4 wq1 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r1, ch, 64));
         const uint4 wk0 = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(r0, ch, 64));
@@ -482,27 +482,21 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             unpack_bf16(wg0, g0);
             unpack_bf16(wg1, g1);
             const bool v0 = r0 < L, v1 = r1 < L;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (!v0) g0[i] = 0.f;
-                if (!v1) g1[i] = 0.f;
-            }
-            // inclusive prefix sums over rows 0..31 and 32..63
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float a = __shfl_up_sync(0xffffffffu, g0[i], off);
-                    const float b = __shfl_up_sync(0xffffffffu, g1[i], off);
-                    if (lane >= off) { g0[i] += a; g1[i] += b; }
-                }
-            }
+            // G at rows 2l and 2l+1: inclusive warp scan of the row-pair sums
             float gref[8], glast[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                gref[i] = __shfl_sync(0xffffffffu, g0[i], 31);   // G at row 31
-                g1[i] += gref[i];
-                glast[i] = __shfl_sync(0xffffffffu, g1[i], 31);  // G at row 63 (= last valid row)
+                const float a = v0 ? g0[i] : 0.f, b = v1 ? g1[i] : 0.f;
+                float s2 = a + b;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, s2, off);
+                    if (lane >= off) s2 += t;
+                }
+                g0[i] = s2 - b;   // G at row 2l
+                g1[i] = s2;       // G at row 2l + 1
+                gref[i] = __shfl_sync(0xffffffffu, s2, 15);    // G at row 31
+                glast[i] = __shfl_sync(0xffffffffu, s2, 31);   // G at row 63 (= last valid row)
             }
             bool bad = false;
             float egr[8], elr[8];   // per channel: exp(G_ref), exp(G_L - G_ref)
