@@ -135,22 +135,6 @@ __device__ __forceinline__ void stage_token(TokenIn &in, const T *__restrict__ q
     }
 }
 
-// Stage one stored ring record (the fold's input): k, v in the ring's dtype,
-// decay and beta in fp32 exactly as the verify kernel stored them.
-template <typename T>
-__device__ __forceinline__ void stage_record(TokenIn &in, const T *__restrict__ k,
-                                             const T *__restrict__ v,
-                                             const float *__restrict__ decay,
-                                             const float *__restrict__ beta) {
-    const int t = threadIdx.x;
-    if (t < KD) {
-        in.k[t] = to_f(k[t]);
-        in.alpha[t] = decay[t];
-        in.v[t] = to_f(v[t]);
-        if (t == 0) in.beta = beta[0];
-    }
-}
-
 // One token of the recurrence on the CTA's register-resident state.
 // Requires every thread of the CTA; `in` must be visible (synchronised).  With
 // OUT, threads 0..127 return o[threadIdx.x] (already multiplied by scale).

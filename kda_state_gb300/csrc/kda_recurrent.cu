@@ -47,18 +47,15 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) decode_kernel(DecodeArgs a) {
 // verify: G draft tokens from the committed state, which is never written;
 // record i goes to ring entry (base + i) mod R of the request's slot.
 // ---------------------------------------------------------------------------
+
+// Recurrent form: the G tokens one after another on a register copy of the
+// state (the decode arithmetic).  Used for G > 16 and as the fallback of the
+// draft-block form below.
 template <typename T>
-__global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__device__ __forceinline__ void verify_unit_recurrent(const VerifyArgs &a, int b, int h, int slot,
+                                                      unsigned char *smem) {
     Reduce &red = *reinterpret_cast<Reduce *>(smem);
     TokenIn *in = reinterpret_cast<TokenIn *>(smem + sizeof(Reduce));
-    const int unit = blockIdx.x;
-    const int b = unit / a.H, h = unit - b * a.H;
-    const int slot = a.slot_ids[b];
-    if (slot < 0 || slot >= a.num_slots) {
-        if (threadIdx.x == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
-        return;
-    }
     StateRegs r;
     state_load(r, a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS);
     const int base = a.ring_base ? a.ring_base[b] : 0;
@@ -76,6 +73,223 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
         const float o = token_update<true>(r, in[i], red, a.scale);
         if (threadIdx.x < VD)
             ((T *)a.o)[(((size_t)b * a.G + i) * a.H + h) * VD + threadIdx.x] = from_f<T>(o);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int unit = blockIdx.x;
+    const int b = unit / a.H, h = unit - b * a.H;
+    const int slot = a.slot_ids[b];
+    if (slot < 0 || slot >= a.num_slots) {
+        if (threadIdx.x == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
+        return;
+    }
+    verify_unit_recurrent<T>(a, b, h, slot, smem);
+}
+
+// Draft-block form (G <= GM): all G outputs from h0 at once.  With
+// E_r = exp(sum_{j<=r} gk_j) (the product of the step decays) per key channel,
+//     A[r][j]   = b_r <k_r E_r, k_j / E_j>   (j < r),   T = (I + A)^-1
+//     Aqk[r][j] = <q_r E_r, k_j / E_j>       (j <= r)
+//     W = T Diag(b) (K . E),  U~ = T Diag(b) V,  U = U~ - W h0
+//     O = (Q . E) h0 + Aqk U
+// The state is read once; the G x 128 x 128 products with h0 run on the CUDA
+// cores in fp32 (2G vectors against the register-resident h0).  A unit whose
+// decay over the draft leaves fp32 range for 1/E falls back to the recurrent
+// form.  Thread mapping for h0: warp w owns columns 16w .. 16w+15, lane l
+// column 16w + (l & 15) and rows 64 (l >> 4) .. + 63.
+template <int GM>
+struct VerifyBlockSmem {
+    float kg[GM][KD];   // k . E
+    float kn[GM][KD];   // k / E
+    float qg[GM][KD];   // q . E
+    float v[GM][VD];
+    float w[GM][KD];    // W
+    float ut[GM][VD];   // U~
+    float akk[GM][GM], aqk[GM][GM], tb[GM][GM];
+    float beta[GM];
+    int fallback;
+};
+
+template <typename T, int GM>
+__global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    VerifyBlockSmem<GM> &sm = *reinterpret_cast<VerifyBlockSmem<GM> *>(smem);
+    const int unit = blockIdx.x;
+    const int b = unit / a.H, h = unit - b * a.H;
+    const int G = a.G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = a.slot_ids[b];
+    if (slot < 0 || slot >= a.num_slots) {
+        if (tid == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
+        return;
+    }
+    // h0 into registers (read-only): column c, rows 64*hr .. 64*hr + 63
+    const int col = 16 * warp + (lane & 15), hr = lane >> 4;
+    const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS + (size_t)(64 * hr) * VD + col;
+    float s[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)i * VD);
+
+    if (tid == 0) sm.fallback = 0;
+    const int base = a.ring_base ? a.ring_base[b] : 0;
+    const int mask = a.ring_len - 1;
+    // stage the draft, store the records; running decay products per channel.
+    // All loads of the draft are issued before the first store.
+    if (tid < KD) {
+        const int c = tid;
+        T kr[GM], qr[GM], gr[GM];
+#pragma unroll
+        for (int i = 0; i < GM; ++i) {
+            if (i < G) {
+                const size_t tok = ((size_t)b * G + i) * a.H + h;
+                kr[i] = ((const T *)a.k)[tok * KD + c];
+                qr[i] = ((const T *)a.q)[tok * KD + c];
+                gr[i] = ((const T *)a.gk)[tok * KD + c];
+            }
+        }
+        float E = 1.f;
+        bool tiny = false;
+#pragma unroll
+        for (int i = 0; i < GM; ++i) {
+            if (i < G) {
+                const size_t e = ((size_t)slot * a.ring_len + ((base + i) & mask)) * a.H + h;
+                const float alpha = expf(to_f(gr[i]));
+                ((T *)a.rk)[e * KD + c] = kr[i];
+                a.rdecay[e * KD + c] = alpha;
+                E *= alpha;
+                tiny |= !(E > 1e-30f);
+                const float kk = to_f(kr[i]), qq = to_f(qr[i]);
+                sm.kg[i][c] = kk * E;
+                sm.kn[i][c] = kk / E;
+                sm.qg[i][c] = qq * E;
+            }
+        }
+        if (tiny) sm.fallback = 1;
+    } else {
+        const int c = tid - KD;
+        T vr[GM], br[GM];
+#pragma unroll
+        for (int i = 0; i < GM; ++i) {
+            if (i < G) {
+                const size_t tok = ((size_t)b * G + i) * a.H + h;
+                vr[i] = ((const T *)a.v)[tok * VD + c];
+                if (c == 0) br[i] = ((const T *)a.beta)[tok];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < GM; ++i) {
+            if (i < G) {
+                const size_t e = ((size_t)slot * a.ring_len + ((base + i) & mask)) * a.H + h;
+                ((T *)a.rv)[e * VD + c] = vr[i];
+                sm.v[i][c] = to_f(vr[i]);
+                if (c == 0) {
+                    const float bb = to_f(br[i]);
+                    a.rbeta[e] = bb;
+                    sm.beta[i] = bb;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (sm.fallback) {
+        // The records above are the same ones the recurrent form stores; it
+        // rewrites them identically.
+        __syncthreads();
+        verify_unit_recurrent<T>(a, b, h, slot, smem);
+        return;
+    }
+    // Gram entries: pair p -> (r, j); pairs [0, G(G-1)/2) are A, the rest Aqk
+    const int nkk = G * (G - 1) / 2, npairs = nkk + G * (G + 1) / 2;
+    for (int pidx = warp; pidx < npairs; pidx += CTA_WARPS) {
+        int r, j;
+        const bool is_kk = pidx < nkk;
+        {
+            int q = is_kk ? pidx : pidx - nkk;   // enumerate rows of a lower triangle
+            r = is_kk ? 1 : 0;
+            while (q >= (is_kk ? r : r + 1)) { q -= (is_kk ? r : r + 1); ++r; }
+            j = q;
+        }
+        const float4 x = reinterpret_cast<const float4 *>(is_kk ? sm.kg[r] : sm.qg[r])[lane];
+        const float4 y = reinterpret_cast<const float4 *>(sm.kn[j])[lane];
+        float d = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (lane == 0) {
+            if (is_kk) sm.akk[r][j] = d * sm.beta[r];
+            else sm.aqk[r][j] = d;
+        }
+    }
+    __syncthreads();
+    // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b)
+    if (warp == 0 && lane < G) {
+        const int cc = lane;
+        float x[GM];
+#pragma unroll
+        for (int r = 0; r < GM; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < GM; ++r) {
+            if (r < G && r > cc) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < GM; ++j)
+                    if (j < r) acc = fmaf(sm.akk[r][j], x[j], acc);
+                x[r] = -acc;
+            }
+        }
+        for (int r = 0; r < G; ++r) sm.tb[r][cc] = (r >= cc) ? x[r] * sm.beta[cc] : 0.f;
+    }
+    __syncthreads();
+    // W = T Diag(b) (K . E) and U~ = T Diag(b) V, one column per thread
+    {
+        const int c = tid & (KD - 1);
+        const bool do_w = tid < KD;
+        for (int r = 0; r < G; ++r) {
+            float acc = 0.f;
+            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
+            if (do_w) sm.w[r][c] = acc;
+            else sm.ut[r][c] = acc;
+        }
+    }
+    __syncthreads();
+    // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
+    // the other row half via one shuffle.  acc[i] (i < GM) is row i of W,
+    // acc[GM + i] row i of Q . E.
+    float acc[2 * GM];
+#pragma unroll
+    for (int i = 0; i < 2 * GM; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int k4 = 0; k4 < 16; ++k4) {
+        const int k = 64 * hr + 4 * k4;
+#pragma unroll
+        for (int i = 0; i < 2 * GM; ++i) {
+            if ((i < GM ? i : i - GM) < G) {
+                const float *row = (i < GM) ? sm.w[i] : sm.qg[i - GM];
+                const float4 x = *reinterpret_cast<const float4 *>(row + k);
+                acc[i] = fmaf(x.x, s[4 * k4], acc[i]);
+                acc[i] = fmaf(x.y, s[4 * k4 + 1], acc[i]);
+                acc[i] = fmaf(x.z, s[4 * k4 + 2], acc[i]);
+                acc[i] = fmaf(x.w, s[4 * k4 + 3], acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2 * GM; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
+    // U = U~ - W h0;  O = (Q . E) h0 + Aqk U;  each row half writes half the rows
+    float u[GM];
+#pragma unroll
+    for (int r = 0; r < GM; ++r) u[r] = (r < G) ? sm.ut[r][col] - acc[r] : 0.f;
+    const int half = (G + 1) / 2;
+#pragma unroll
+    for (int r = 0; r < GM; ++r) {
+        if (r < G && ((r < half) == (hr == 0))) {
+            float o = acc[GM + r];
+#pragma unroll
+            for (int j = 0; j <= r; ++j) o = fmaf(sm.aqk[r][j], u[j], o);
+            ((T *)a.o)[(((size_t)b * G + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
+        }
     }
 }
 
@@ -108,10 +322,33 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) fold_kernel(const __grid_const
     state_load(r, S);
     const int base = p.ring_base ? p.ring_base[b] : 0;
     const int mask = p.ring_len - 1;
-    for (int i = 0; i < acc; ++i) {
-        const size_t e = ((size_t)slot * p.ring_len + ((base + i) & mask)) * p.H + h;
-        stage_record<T>(in[i], (const T *)L.rk + e * KD, (const T *)L.rv + e * VD,
-                        L.rdecay + e * KD, L.rbeta + e);
+    // stage the records in batches of 8, every load of a batch issued first
+    const int t = threadIdx.x;
+    if (t < KD) {
+        for (int i0 = 0; i0 < acc; i0 += 8) {
+            T kr[8], vr[8];
+            float dr[8], br[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (i0 + j < acc) {
+                    const size_t e = ((size_t)slot * p.ring_len + ((base + i0 + j) & mask)) * p.H + h;
+                    kr[j] = ((const T *)L.rk)[e * KD + t];
+                    vr[j] = ((const T *)L.rv)[e * VD + t];
+                    dr[j] = L.rdecay[e * KD + t];
+                    if (t == 0) br[j] = L.rbeta[e];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (i0 + j < acc) {
+                    TokenIn &x = in[i0 + j];
+                    x.k[t] = to_f(kr[j]);
+                    x.alpha[t] = dr[j];
+                    x.v[t] = to_f(vr[j]);
+                    if (t == 0) x.beta = br[j];
+                }
+            }
+        }
     }
     __syncthreads();
     for (int i = 0; i < acc; ++i) token_update<false>(r, in[i], red, 1.f);
@@ -182,11 +419,27 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename T, int GM>
+cudaError_t launch_verify_block(const VerifyArgs &a, cudaStream_t s) {
+    const unsigned grid = (unsigned)a.B * (unsigned)a.H;
+    const size_t rec = sizeof(Reduce) + (size_t)a.G * sizeof(TokenIn);   // fallback's needs
+    const size_t smem = sizeof(VerifyBlockSmem<GM>) > rec ? sizeof(VerifyBlockSmem<GM>) : rec;
+    cudaError_t e = set_smem(verify_block_kernel<T, GM>, smem);
+    if (e != cudaSuccess) return e;
+    verify_block_kernel<T, GM><<<grid, CTA_THREADS, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s) {
+    const bool bf = a.dt == KDA_DTYPE_BF16;
+    if (a.G <= 8)
+        return bf ? launch_verify_block<__nv_bfloat16, 8>(a, s) : launch_verify_block<float, 8>(a, s);
+    if (a.G <= 16)
+        return bf ? launch_verify_block<__nv_bfloat16, 16>(a, s) : launch_verify_block<float, 16>(a, s);
     const unsigned grid = (unsigned)a.B * (unsigned)a.H;
     const size_t smem = sizeof(Reduce) + (size_t)a.G * sizeof(TokenIn);
     cudaError_t e;
-    if (a.dt == KDA_DTYPE_BF16) {
+    if (bf) {
         if ((e = set_smem(verify_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
         verify_kernel<__nv_bfloat16><<<grid, CTA_THREADS, smem, s>>>(a);
     } else {

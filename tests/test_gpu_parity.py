@@ -304,3 +304,30 @@ def test_device_errors_are_reported_and_skipped():
                             pool, sl, sl, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & kda().KDA_DEVERR_SEQLENS
+
+
+@pytest.mark.parametrize("case", ["strong_decay_fallback", "long_draft_recurrent"])
+def test_verify_other_paths(case):
+    """Verify's other code paths: a draft whose cumulative decay leaves the
+    range of the block form (gk = -12 per step), and G = 20 > 16 drafts."""
+    g = gen.make_gen(61)
+    B, H, S = 3, 2, 6
+    G, R = (8, 16) if case == "strong_decay_fallback" else (20, 64)
+    x = gen.token_inputs(G, H, torch.bfloat16, g, lead=(B,))
+    if case == "strong_decay_fallback":
+        x["gk"] = torch.full_like(x["gk"], -12.0)
+    pool = gen.checkpoint((S, H, KD, VD), g).to(DEV)
+    committed = pool.clone()
+    ids = torch.tensor([4, 0, 2], dtype=torch.int32, device=DEV)
+    ring = kda().make_ring(S, R, H, torch.bfloat16, DEV)
+    xd = _dev(x)
+    o = kda().kda_verify_store_inputs(xd["q"], xd["k"], xd["v"], xd["gk"], xd["beta"], ids, pool, ring)
+    torch.cuda.synchronize()
+    assert torch.equal(pool, committed)
+    o_ref = oracle.verify(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["gk"]), f64(x["beta"]),
+                          f64(committed[ids.long()]))
+    assert_close(o, o_ref, torch.bfloat16, "verify o")
+    for b in range(B):
+        s = int(ids[b])
+        assert torch.equal(ring.k[s, :G].cpu(), x["k"][b])
+        assert torch.equal(ring.beta[s, :G].cpu(), x["beta"][b].float())
