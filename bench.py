@@ -351,9 +351,9 @@ class OracleVarlen:
 # main
 # ---------------------------------------------------------------------------
 
-def profile_traffic(kernel_src, summary_name):
-    """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (matched by hash)."""
+def profile_traffic(kernel_src, summary_name, key="dram_bytes_per_launch"):
+    """DRAM bytes (read + write) from a committed ncu summary, if it was taken
+    on the current kernel source (matched by hash); else None."""
     path = os.path.join(ROOT, "profiles", summary_name)
     try:
         txt = open(path).read()
@@ -361,7 +361,7 @@ def profile_traffic(kernel_src, summary_name):
         return None
     h = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()[:12]
     m_h = re.search(r"source_sha1:\s*([0-9a-f]+)", txt)
-    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m_t = re.search(key + r":\s*([0-9.eE+]+)", txt)
     if not m_h or not m_t or m_h.group(1) != h:
         return None
     return float(m_t.group(1))
@@ -403,6 +403,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--only", choices=["decode", "verify"], default=None,
                     help="run one of the secondary workloads alone (for profiling)")
+    ap.add_argument("--layers", type=int, default=69,
+                    help="layers of the --only workload (a smaller case for profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
@@ -413,7 +415,7 @@ def main():
         from kda_state_gb300 import _build
         _build.build()
         fn = bench_decode if args.only == "decode" else bench_verify_fold
-        r = fn(args, 1, steps=args.steps)
+        r = fn(args, 1, layers=args.layers, steps=args.steps)
         print(json.dumps({"only": args.only, **{k: v for k, v in r.items()
                                                  if isinstance(v, (int, float))}}), flush=True)
         return
@@ -427,11 +429,17 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu:
         try:
             orc = OracleVarlen()
-            nh = orc.heads_for(15.0)
-            r, dt = orc.rate(nh)
-            cpu = {"value": r, "unit": "tok/s", "cores": orc.threads, "kind": "oracle",
-                   "sample": "%d (sequence, head) units (8 sequences x %d of 64 heads), %d "
-                             "token-heads, %.1f s" % (8 * nh, nh, orc.T * nh, dt)}
+            nh = orc.heads_for(10.0)
+            tok, secs, passes = 0.0, 0.0, 0
+            while secs < 10.0 and passes < 50:     # repeat the sample to about 10 s
+                r, dt = orc.rate(nh)
+                tok += r * dt
+                secs += dt
+                passes += 1
+            cpu = {"value": tok / secs, "unit": "tok/s", "cores": orc.threads, "kind": "oracle",
+                   "sample": "%d pass(es) over %d (sequence, head) units (8 sequences x %d of 64 "
+                             "heads, %d token-heads each), %.1f s" % (passes, 8 * nh, nh, orc.T * nh,
+                                                                      secs)}
         except Exception as e:  # noqa: BLE001
             cpu = {"value": None, "unit": "tok/s", "cores": None, "kind": "oracle",
                    "sample": "failed: %s" % e}
@@ -449,7 +457,7 @@ def main():
     value = res["T"] / (ms / 1e3) * ws
     achieved = res["alg_bytes"] / (ms / 1e3) / 1e9
     src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_prefill_tc.cu")
-    traffic = profile_traffic(src, "prefill_varlen.md") if os.path.exists(src) else None
+    traffic = profile_traffic(src, "prefill_tc_kernel.varlen.md")
     line = {
         "metric": "KDA prefill tok/s (varlen chunked prefill)",
         "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -470,6 +478,7 @@ def main():
         "cpu_baseline": cpu,
     }
     if not args.no_also:
+        rec_src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_recurrent.cu")
         also = {}
         try:
             d = bench_decode(args, ws)
@@ -480,6 +489,7 @@ def main():
                 "decode_kernel_us": d["dec_ms"] * 1e3,
                 "decode_kernel_GBps": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9,
                 "decode_kernel_frac": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9 / hbm,
+                "decode_kernel_traffic": profile_traffic(rec_src, "decode_kernel.decode.md"),
                 "step_GBps": (d["dec_bytes"] + d["cow_bytes"]) * d["layers"] / (d["ms"] / 1e3) / 1e9,
             }
         except Exception as e:  # noqa: BLE001
@@ -494,6 +504,8 @@ def main():
                 "verify_kernel_us": v["ver_ms"] * 1e3,
                 "verify_kernel_GBps": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9,
                 "verify_kernel_frac": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9 / hbm,
+                "verify_kernel_traffic": profile_traffic(
+                    rec_src, "verify_block_kernel_fold_kernel.verify.md", "verify_dram_bytes_per_launch"),
                 "fold_kernel_us": v["fold_ms"] * 1e3,
                 "fold_kernel_GBps": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9,
                 "fold_kernel_frac": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9 / hbm,
