@@ -31,12 +31,12 @@
 //   G3  [-W; Q~] (128x128) x S0 (+=)        -> cols [128,256): U (rows 0-63), Q~ S0 (64-127)
 //   G4a [0; Aqk] (128x64) x U (+=)          -> cols [128,256): rows 64-127 become O
 //   G4b (K . exp(G_L - G))^T (128x64) x U   -> cols [0,128): the state increment
-// Operand precision: the Gram factors span exp(+-26) and need bf16's range,
-// so G1 runs as three bf16 products (hi*hi + lo*hi + hi*lo of a hi/lo split,
-// ~16-bit significands); G2 takes V as given (bf16); the operands of G3 and G4
-// are bounded (|.| <= 1 for the decayed q, k and Aqk; U, W and S are checked
-// against 60000) and use fp16's 11-bit significand.  Rounding all operands to
-// bf16 instead gives 3e-2 x RMS on o, fp16 + split G1 about 3e-3.
+// Operand precision: the Gram factors span exp(+-26) and need an 8-bit
+// exponent, so G1 runs on TF32 (fp32 operands, 11-bit significands); G2 takes V
+// as given (bf16); the operands of G3 and G4 are bounded (|.| <= 1 for the
+// decayed q, k and Aqk; U, W and S are checked against 60000) and use fp16's
+// 11-bit significand.  Rounding all operands to bf16 instead gives 3e-2 x RMS
+// on o; this mix about 3e-3.
 // CUDA cores do the cumulative decays, the exponentials, the 64x64 unit-lower
 // triangular inverse (16x16 blocks), the TMEM read-outs and the fp32 state
 // update.  All waits are bounded; a wait that gives up reports
@@ -65,15 +65,14 @@ constexpr int AS = 68;             // row stride (floats) of the fp32 A scratch
 // then the next chunk's raw q, k, gk (TMA), the triangular-solve scratch and
 // the [T Diag(b); 0; Aqk] tile.  The prep reads its raw tiles into registers
 // before it overwrites R1.
-constexpr uint32_t OP_A1H = 0;         // [Kf; Qr] hi, bf16, 128 rows x 128 ch, K-major A
-constexpr uint32_t OP_A1L = 32768;     // [Kf; Qr] lo
-constexpr uint32_t OP_B1H = 65536;     // Kb hi, bf16, 64 rows x 128 ch, K-major B
-constexpr uint32_t OP_B1L = 81920;     // Kb lo
+constexpr uint32_t OP_A1 = 0;          // [Kf; Qr], fp32 (tf32 MMA), 128 rows x 128 ch, K-major A
+constexpr uint32_t OP_B1 = 65536;      // Kb, fp32, 64 rows x 128 ch, K-major B
 constexpr uint32_t RAW_Q = 0;          // 64 tokens x 128 ch bf16, 2 boxes of 64 ch (TMA)
 constexpr uint32_t RAW_K = 16384;
 constexpr uint32_t RAW_G = 32768;
 constexpr uint32_t SCR_A = 49152;      // fp32 A [64][AS]
 constexpr uint32_t OP_TBZ = 69632;     // rows 0-63 T Diag(b) (bf16), 64-127 zero, 128-191 Aqk (fp16)
+constexpr uint32_t SCR_RW = 94208;     // per-warp R scratch of the solve (3 x 16 x RW floats)
 constexpr uint32_t R1_END = 98304;
 constexpr uint32_t RAW_V = 98304;      // v, bf16, also the MN-major B operand of U~ = T Diag(b) V
 constexpr uint32_t OP_KT = 114688;     // K . exp(G), bf16, 64 tokens x 128 ch, MN-major B
@@ -83,13 +82,13 @@ constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 12
 constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
 constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
 constexpr uint32_t SM_BETA = 229376;   // fp32 [64]
-constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [128]: exp(G_L)
-constexpr uint32_t SM_BAR = SM_GAM + 512;    // 3 mbarriers
+constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [2][128]: exp(G_L), by chunk parity
+constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 3 mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 static_assert(SCR_A + 64 * AS * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
-static_assert(3 * 16 * 24 * 4 <= 8192, "R scratch overflows TBZ rows 0-63");
+static_assert(OP_TBZ + 192 * 128 <= SCR_RW && SCR_RW + 3 * 16 * 20 * 4 <= R1_END, "R scratch misplaced");
 static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 
@@ -173,8 +172,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor, kind::f16, fp32 accumulate; fmt 1 = bf16, 0 = fp16
-// (A and B always share one format).
+// Instruction descriptor, fp32 accumulate; fmt 1 = bf16, 0 = fp16 (kind::f16),
+// 2 = tf32 (kind::tf32).  A and B always share one format.
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn, int fmt) {
     return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)a_mn << 15) |
            ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -183,6 +182,12 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d),
         "l"(a), "l"(b), "r"(id), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -221,6 +226,19 @@ __device__ __forceinline__ void tmem_wait_ld() {
 __device__ __forceinline__ uint32_t chunk_off(int row, int col, int rows) {
     return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4));
 }
+// Byte offset of the 16-byte chunk holding fp32 columns col..col+3 (col % 4 ==
+// 0) of a tile of `rows` rows x 128 fp32 columns stored as four boxes of 32
+// columns (rows x 128 B each, 128-byte swizzle).
+__device__ __forceinline__ uint32_t chunk32_off(int row, int col, int rows) {
+    return (uint32_t)((col >> 5) * rows * 128 + row * 128 + ((((col >> 2) & 7) ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ void store_f32x8(uint8_t *base, uint32_t tile, int row, int col, int rows,
+                                            const float *v8) {
+    *reinterpret_cast<float4 *>(base + tile + chunk32_off(row, col, rows)) =
+        make_float4(v8[0], v8[1], v8[2], v8[3]);
+    *reinterpret_cast<float4 *>(base + tile + chunk32_off(row, col + 4, rows)) =
+        make_float4(v8[4], v8[5], v8[6], v8[7]);
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -238,18 +256,6 @@ __device__ __forceinline__ void store_f16(uint8_t *base, uint32_t off, const flo
     *reinterpret_cast<uint4 *>(base + off) =
         make_uint4(pack_f16x2(v8[0], v8[1]), pack_f16x2(v8[2], v8[3]), pack_f16x2(v8[4], v8[5]),
                    pack_f16x2(v8[6], v8[7]));
-}
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): two bf16 chunks.
-__device__ __forceinline__ void store_bf16_split(uint8_t *base, uint32_t off_hi, uint32_t off_lo,
-                                                 const float *v8) {
-    float hi[8], lo[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        hi[i] = __bfloat162float(__float2bfloat16_rn(v8[i]));
-        lo[i] = v8[i] - hi[i];
-    }
-    store_bf16(base, off_hi, hi);
-    store_bf16(base, off_lo, lo);
 }
 __device__ __forceinline__ void unpack_bf16(const uint4 &w, float *v8) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
@@ -297,10 +303,19 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-constexpr int RW = 24;   // row stride (floats) of a warp's 16 x 16 R scratch
+constexpr int RW = 20;   // row stride (floats) of a warp's 16 x 16 R scratch
+
+// T Diag(beta) element pair (r, c), (r, c + 1), c even, as bf16 into the
+// K-major [T Diag(b); 0; Aqk] tile (64 token columns, one 128-byte row per r).
+__device__ __forceinline__ void store_tb2(uint8_t *tbz, int r, int c, float t0, float t1,
+                                          const float *beta) {
+    *reinterpret_cast<uint32_t *>(tbz + r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2) =
+        pack_bf16x2(t0 * beta[c], t1 * beta[c + 1]);
+}
 
 template <int J>
-__device__ __forceinline__ void solve_block_column(const float *As, float *Ts, float *Rw, int lane) {
+__device__ __forceinline__ void solve_block_column(const float *As, float *Ts, float *Rw, int lane,
+                                                   uint8_t *tbz, const float *beta) {
     const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int I = J + 1; I < 4; ++I) {
@@ -350,6 +365,9 @@ __device__ __forceinline__ void solve_block_column(const float *As, float *Ts, f
             Ts[(16 * I + g) * 64 + c + 1] = -tc[nt][1];
             Ts[(16 * I + g + 8) * 64 + c] = -tc[nt][2];
             Ts[(16 * I + g + 8) * 64 + c + 1] = -tc[nt][3];
+            const int cl = 16 * J + 8 * nt + 2 * t4;
+            store_tb2(tbz, 16 * I + g, cl, -tc[nt][0], -tc[nt][1], beta);
+            store_tb2(tbz, 16 * I + g + 8, cl, -tc[nt][2], -tc[nt][3], beta);
         }
         __syncwarp();
     }
@@ -368,7 +386,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *beta_s = reinterpret_cast<float *>(sm + SM_BETA);
     float *gam_s = reinterpret_cast<float *>(sm + SM_GAM);
     float *As = reinterpret_cast<float *>(sm + SCR_A);
-    float *Rws = reinterpret_cast<float *>(sm + OP_TBZ);   // per-warp R scratch until TB is written
+    float *Rws = reinterpret_cast<float *>(sm + SCR_RW);   // per-warp R scratch of the solve
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
                    bar_mma = sbase + SM_BAR + 16;
@@ -446,7 +464,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float beta_next = 0.f;
     if (tid < C && nchunks > 0 && tid < min(C, eos - bos))
         beta_next = __bfloat162float(p.beta[(size_t)(bos + tid) * p.H + h]);
-    constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 1);
+    constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 2);
     constexpr uint32_t ID_G2 = idesc(128, 128, 0, 1, 1);
     constexpr uint32_t ID_G3 = idesc(128, 128, 0, 1, 0);
     constexpr uint32_t ID_G4A = idesc(128, 128, 0, 1, 0);
@@ -528,10 +546,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                     qr[i] = q_ * ef;
                     qt[i] = q_ * (egr[i] * ef);              // q exp(G_r)
                 }
-                store_bf16_split(sm, OP_A1H + chunk_off(r, ch, 128), OP_A1L + chunk_off(r, ch, 128), kf);
-                store_bf16_split(sm, OP_A1H + chunk_off(64 + r, ch, 128),
-                                 OP_A1L + chunk_off(64 + r, ch, 128), qr);
-                store_bf16_split(sm, OP_B1H + chunk_off(r, ch, 64), OP_B1L + chunk_off(r, ch, 64), kb);
+                store_f32x8(sm, OP_A1, r, ch, 128, kf);
+                store_f32x8(sm, OP_A1, 64 + r, ch, 128, qr);
+                store_f32x8(sm, OP_B1, r, ch, 64, kb);
                 store_bf16(sm, OP_KT + chunk_off(r, ch, 64), kt);
                 store_f16(sm, OP_KE + chunk_off(r, ch, 64), ke);
                 store_f16(sm, OP_A3 + chunk_off(64 + r, ch, 128), qt);
@@ -539,24 +556,19 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             if (bad) atomicOr(flags, FLAG_RANGE);
             if (lane == 31) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) gam_s[ch + i] = expf(glast[i]);
+                for (int i = 0; i < 8; ++i) gam_s[(c & 1) * 128 + ch + i] = expf(glast[i]);
             }
         }
         fence_proxy_async();
         __syncthreads();
 
-        // (3) G1 as hi*hi + lo*hi + hi*lo
+        // (3) G1 on TF32: [Kf; Qr] Kb^T, 16 steps of K = 8
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int t = 0; t < 3; ++t) {
-                const uint32_t a0 = sbase + (t == 1 ? OP_A1L : OP_A1H);
-                const uint32_t b0 = sbase + (t == 2 ? OP_B1L : OP_B1H);
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma(tmem, sdesc(a0 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
-                        sdesc(b0 + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), ID_G1, (t | s) != 0);
-            }
+            for (int s = 0; s < 16; ++s)
+                mma_tf32(tmem, sdesc(sbase + OP_A1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                         sdesc(sbase + OP_B1 + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), ID_G1, s > 0);
             mma_commit(bar_mma);
         }
 
@@ -616,26 +628,37 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 }
                 if (r > col) x[r] = -(a0 + a1);
             }
+            const int c = 16 * I + col;
+            const float bc = beta_s[c];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * 64 + tsw(r, 16 * I + col)] = x[r];
-        }
-        __syncthreads();
-        if (warp == 0) solve_block_column<0>(As, Ts, Rws, lane);
-        else if (warp == 1) solve_block_column<1>(As, Ts, Rws + 16 * RW, lane);
-        else if (warp == 2) solve_block_column<2>(As, Ts, Rws + 32 * RW, lane);
-        __syncthreads();
-        // T Diag(beta) -> bf16 rows 0..63 of TBZ; rows 64..127 zero
-        {
-            const int r = tid >> 3, cc = tid & 7;
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int col = 8 * cc + j;
-                v[j] = ((col >> 4) <= (r >> 4)) ? Ts[r * 64 + tsw(r, col)] * beta_s[col] : 0.f;
+            for (int r = 0; r < 16; ++r) {
+                const int rr = 16 * I + r;
+                Ts[rr * 64 + tsw(r, c)] = x[r];
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OP_TBZ + rr * 128 + ((((c >> 3) ^ rr) & 7) << 4) +
+                                                   (c & 7) * 2) = __float2bfloat16_rn(x[r] * bc);
             }
-            store_bf16(sm, OP_TBZ + (uint32_t)r * 128 + (((cc ^ r) & 7) << 4), v);
-            *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * tid) = make_uint4(0, 0, 0, 0);
+        } else if (warp >= 4) {
+            // zero blocks above the diagonal of T Diag(b) and the zero rows 64..127
+            const int t = tid - 128;                   // 0 .. 383
+            *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * t) = make_uint4(0, 0, 0, 0);
+            if (t < 128) *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * (384 + t)) = make_uint4(0, 0, 0, 0);
+            if (t < 96) {   // 6 upper blocks x 16 rows, two 16-byte chunks each
+                const int blk = t >> 4, r = t & 15;
+                const int I = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
+                const int J = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                const int rr = 16 * I + r;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int cchunk = 2 * J + h2;
+                    *reinterpret_cast<uint4 *>(sm + OP_TBZ + rr * 128 + (((cchunk ^ rr) & 7) << 4)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
         }
+        __syncthreads();
+        if (warp == 0) solve_block_column<0>(As, Ts, Rws, lane, sm + OP_TBZ, beta_s);
+        else if (warp == 1) solve_block_column<1>(As, Ts, Rws + 16 * RW, lane, sm + OP_TBZ, beta_s);
+        else if (warp == 2) solve_block_column<2>(As, Ts, Rws + 32 * RW, lane, sm + OP_TBZ, beta_s);
         fence_proxy_async();
         __syncthreads();
 
@@ -737,7 +760,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             uint32_t r[32];
             KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
             tmem_wait_ld();
-            const float gm = gam_s[srow];
+            const float gm = gam_s[(c & 1) * 128 + srow];
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = fmaf(gm, S[j], __uint_as_float(r[j]));
             if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
@@ -745,11 +768,17 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             for (int j = 0; j < 4; ++j)
                 store_f16(sm, OP_S + chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
         }
+        // No block barrier here: each warp goes on to the next chunk's loads
+        // and scan.  The next chunk's first barrier orders these TMEM reads
+        // before G1 overwrites the columns, and these S stores before G3 reads
+        // them (they reach the MMA's proxy through the fence below).  gam_s is
+        // double-buffered by chunk parity; nothing else this epilogue reads is
+        // written before that barrier.
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
-        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
     }
+    __syncthreads();
+    if (*flags & FLAG_TIMEOUT) aborted = true;
 
     if ((*flags & FLAG_RANGE) && tid == 0) report(p.err, DEVERR_RANGE);
     if (aborted) {
