@@ -100,13 +100,15 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
 // decay over the draft leaves fp32 range for 1/E falls back to the recurrent
 // form.  Thread mapping for h0: warp w owns columns 16w .. 16w+15, lane l
 // column 16w + (l & 15) and rows 64 (l >> 4) .. + 63.
+constexpr int XS = KD + 4;   // padded row stride of W and q . E (conflict-free fragment loads)
+
 template <int GM>
 struct VerifyBlockSmem {
     float kg[GM][KD];   // k . E
     float kn[GM][KD];   // k / E
-    float qg[GM][KD];   // q . E
+    float qg[GM][XS];   // q . E
     float v[GM][VD];
-    float w[GM][KD];    // W
+    float w[GM][XS];    // W
     float ut[GM][VD];   // U~
     float akk[GM][GM], aqk[GM][GM], tb[GM][GM];
     float beta[GM];
@@ -126,12 +128,27 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         if (tid == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
         return;
     }
-    // h0 into registers (read-only): column c, rows 64*hr .. 64*hr + 63
+    // h0 into registers (read-only).  Tensor path (bf16 inputs, G <= 8): the B
+    // fragments of m16n8k8 for this warp's 16 columns, as tf32.  CUDA-core path:
+    // column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
+    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
+    const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS;
     const int col = 16 * warp + (lane & 15), hr = lane >> 4;
-    const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS + (size_t)(64 * hr) * VD + col;
+    const int g = lane >> 2, t4 = lane & 3;
     float s[64];
+    if (TENSOR) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)i * VD);
+        for (int ks = 0; ks < 16; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    s[(ks * 2 + nt) * 2 + e] =
+                        __ldg(S0 + (size_t)(8 * ks + t4 + 4 * e) * VD + 16 * warp + 8 * nt + g);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)(64 * hr + i) * VD + col);
+    }
 
     if (tid == 0) sm.fallback = 0;
     const int base = a.ring_base ? a.ring_base[b] : 0;
@@ -246,14 +263,60 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
     {
         const int c = tid & (KD - 1);
         const bool do_w = tid < KD;
-        for (int r = 0; r < G; ++r) {
+        for (int r = 0; r < GM; ++r) {
             float acc = 0.f;
-            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
-            if (do_w) sm.w[r][c] = acc;
-            else sm.ut[r][c] = acc;
+            if (r < G)
+                for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
+            if (do_w) {
+                sm.w[r][c] = acc;
+                if (r >= G) sm.qg[r][c] = 0.f;
+            } else {
+                sm.ut[r][c] = acc;
+            }
         }
     }
     __syncthreads();
+    if (TENSOR) {
+        // [W; Q . E] (16 x 128) h0 (128 x 16 columns of this warp): 16 k-steps x
+        // 2 n-tiles of m16n8k8 TF32.  Row g of the result is W row g (c[.][0..1])
+        // and (Q . E) row g (c[.][2..3]) at columns 16w + 8nt + 2t4 (+1).
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+            const int k = 8 * ks + t4;
+            const uint32_t af[4] = {tf32_bits(sm.w[g][k]), tf32_bits(sm.qg[g][k]),
+                                    tf32_bits(sm.w[g][k + 4]), tf32_bits(sm.qg[g][k + 4])};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t bf[2] = {tf32_bits(s[(ks * 2 + nt) * 2]), tf32_bits(s[(ks * 2 + nt) * 2 + 1])};
+                mma16n8k8_tf32(c[nt], af, bf);
+            }
+        }
+        // U = U~ - W h0 for row g; O = (Q . E) h0 + Aqk U, U rows from the lanes
+        // holding them (lane 4j + t4)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c0 = 16 * warp + 8 * nt + 2 * t4;
+            const float u0 = sm.ut[g][c0] - c[nt][0], u1 = sm.ut[g][c0 + 1] - c[nt][1];
+            float o0 = c[nt][2], o1 = c[nt][3];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                const float uj0 = __shfl_sync(0xffffffffu, u0, 4 * j + t4);
+                const float uj1 = __shfl_sync(0xffffffffu, u1, 4 * j + t4);
+                if (j <= g && j < G) {
+                    const float aq = sm.aqk[g][j];
+                    o0 = fmaf(aq, uj0, o0);
+                    o1 = fmaf(aq, uj1, o1);
+                }
+            }
+            if (g < G) {
+                T *dst = (T *)a.o + (((size_t)b * G + g) * a.H + h) * VD + c0;
+                dst[0] = from_f<T>(a.scale * o0);
+                dst[1] = from_f<T>(a.scale * o1);
+            }
+        }
+        return;
+    }
     // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
     // the other row half via one shuffle.  acc[i] (i < GM) is row i of W,
     // acc[GM + i] row i of Q . E.
