@@ -210,6 +210,39 @@ def bench_varlen(args, ws, sampler):
                 h2d=h2d, d2h=d2h, launches_per_step=1)
 
 
+def bench_long(args, ws, N=4, T=24576, H=96, piece=4096, steps=None):
+    """Six 4096-token pieces of 4 x 24576 tokens (H = 96), each piece one
+    kda_chunk_prefill over the 4 sequences resuming in place from the working
+    slots, with a snapshot to a slot alternating between two (ping-pong)."""
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    P = T // piece
+    gd = gen.make_gen(1002, dev)
+    xs = [gen.token_inputs(N * piece, H, torch.bfloat16, gd, device=dev) for _ in range(P)]
+    ck = gen.checkpoint((N, H, KD, VD), gd, device=dev)
+    pool = torch.zeros(3 * N, H, KD, VD, device=dev)
+    work = torch.arange(N, dtype=torch.int32, device=dev)
+    snaps = [torch.arange(N, 2 * N, dtype=torch.int32, device=dev),
+             torch.arange(2 * N, 3 * N, dtype=torch.int32, device=dev)]
+    cu = gen.cu_seqlens([piece] * N)
+    cu_d = cu.to(dev)
+    o = torch.empty(N * piece, H, VD, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        pool[:N].copy_(ck)
+        for pc in range(P):
+            x = xs[pc]
+            kda.kda_chunk_prefill(x["q"], x["k"], x["v"], x["gk"], x["beta"], cu_d, cu, pool, work,
+                                  work, snaps[pc % 2], o=o)
+
+    K = steps or max(3, min(args.steps, 10))
+    ms = timed(step, K, 3, ws)
+    alg = P * algorithmic_prefill_bytes(N * piece, H, N, snap=True)
+    del xs, pool
+    torch.cuda.empty_cache()
+    return dict(ms=ms, tokens=N * T, alg_bytes=alg, pieces=P)
+
+
 def bench_decode(args, ws, layers=69, B=384, H=64, slots=512, cow_frac=0.10, steps=None):
     import kda_state_gb300 as kda
     dev = "cuda"
@@ -480,6 +513,18 @@ def main():
     if not args.no_also:
         rec_src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_recurrent.cu")
         also = {}
+        try:
+            lg = bench_long(args, ws)
+            also["long_prefill"] = {
+                "tok_per_s": lg["tokens"] / (lg["ms"] / 1e3) * ws, "ms_per_step": lg["ms"],
+                "workload": "4 seqs x 24576 tok, H=96, bf16, from checkpoints, 6 pieces of 4096 "
+                            "resuming in place, ping-pong snapshot per piece",
+                "GBps": lg["alg_bytes"] / (lg["ms"] / 1e3) / 1e9,
+                "frac": lg["alg_bytes"] / (lg["ms"] / 1e3) / 1e9 / hbm,
+                "note": "step includes a 48 MB checkpoint restore before the first piece",
+            }
+        except Exception as e:  # noqa: BLE001
+            also["long_prefill"] = {"error": repr(e)}
         try:
             d = bench_decode(args, ws)
             also["decode"] = {

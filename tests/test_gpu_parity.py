@@ -331,3 +331,39 @@ def test_verify_other_paths(case):
         s = int(ids[b])
         assert torch.equal(ring.k[s, :G].cpu(), x["k"][b])
         assert torch.equal(ring.beta[s, :G].cpu(), x["beta"][b].float())
+
+
+def test_verify_many_units_mixed():
+    """Many units (more than can be resident at once): normal drafts, drafts on
+    the strong-decay fallback and one out-of-range slot interleaved; every
+    valid unit vs the oracle, the skipped request's outputs untouched."""
+    g = gen.make_gen(62)
+    B, G, H, S, R = 170, 8, 4, 180, 16
+    x = gen.token_inputs(G, H, torch.bfloat16, g, lead=(B,))
+    strong = torch.zeros(B, dtype=torch.bool)
+    strong[::7] = True
+    x["gk"][strong] = -12.0
+    pool = gen.checkpoint((S, H, KD, VD), g).to(DEV)
+    committed = pool.clone()
+    ids = gen.slot_permutation(S, g)[:B].clone()
+    ids[100] = S + 5                                   # out of range: reported and skipped
+    ring = kda().make_ring(S, R, H, torch.bfloat16, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xd = _dev(x)
+    o = torch.full((B, G, H, VD), 7.0, dtype=torch.bfloat16, device=DEV)
+    kda().kda_verify_store_inputs(xd["q"], xd["k"], xd["v"], xd["gk"], xd["beta"], ids.to(DEV), pool,
+                                  ring, o=o, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == kda().KDA_DEVERR_SLOT_RANGE
+    assert torch.equal(pool, committed)
+    assert torch.all(o[100] == 7.0), "the skipped request's outputs were written"
+    valid = [b for b in range(B) if b != 100]
+    vb = torch.tensor(valid)
+    o_ref = oracle.verify(f64(x["q"][vb]), f64(x["k"][vb]), f64(x["v"][vb]), f64(x["gk"][vb]),
+                          f64(x["beta"][vb]), f64(committed[ids[vb].long()]))
+    assert_close(o[vb.to(DEV)], o_ref, torch.bfloat16, "verify o")
+    for b in (0, 1, 7, 169):
+        s = int(ids[b])
+        assert torch.equal(ring.k[s, :G].cpu(), x["k"][b])
+        assert torch.equal(ring.v[s, :G].cpu(), x["v"][b])
+        np.testing.assert_allclose(f64(ring.decay[s, :G]), np.exp(f64(x["gk"][b])), rtol=5e-7, atol=0)
