@@ -72,7 +72,7 @@ constexpr uint32_t RAW_K = 16384;
 constexpr uint32_t RAW_G = 32768;
 constexpr uint32_t SCR_A = 49152;      // fp32 A [64][AS]
 constexpr uint32_t OP_TBZ = 69632;     // rows 0-63 T Diag(b) (bf16), 64-127 zero, 128-191 Aqk (fp16)
-constexpr uint32_t SCR_RW = 94208;     // per-warp R scratch of the solve (3 x 16 x RW floats)
+constexpr uint32_t SCR_RW = 94208;     // per-warp R scratch of the solve (6 x 16 x RW floats)
 constexpr uint32_t R1_END = 98304;
 constexpr uint32_t RAW_V = 98304;      // v, bf16, also the MN-major B operand of U~ = T Diag(b) V
 constexpr uint32_t OP_KT = 114688;     // K . exp(G), bf16, 64 tokens x 128 ch, MN-major B
@@ -88,7 +88,7 @@ constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 static_assert(SCR_A + 64 * AS * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
-static_assert(OP_TBZ + 192 * 128 <= SCR_RW && SCR_RW + 3 * 16 * 20 * 4 <= R1_END, "R scratch misplaced");
+static_assert(OP_TBZ + 192 * 128 <= SCR_RW && SCR_RW + 6 * 16 * 8 * 4 <= R1_END, "R scratch misplaced");
 static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 
@@ -283,7 +283,7 @@ __device__ __forceinline__ float absmax(const float *v, int n) {
 // 64 x 64 unit-lower-triangular inverse, off-diagonal blocks.
 // A is fp32 [64][AS] (strictly lower, rows scaled by beta); T is fp32 [64][64]
 // with its columns XOR-swizzled by row: T[r][c] lives at r*64 + tsw(r, c).
-// Warp J owns block column J: for I = J+1 .. 3 it forms
+// Block column J belongs to two warps (8 columns each): for I = J+1 .. 3 they form
 //     R = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II R
 // from blocks of lower levels only, so the warps need no block-wide barrier.
 // The 16 x 16 x 16 products run as warp-level m16n8k8 TF32 MMAs (fp32
@@ -303,7 +303,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-constexpr int RW = 20;   // row stride (floats) of a warp's 16 x 16 R scratch
+constexpr int RW = 8;    // row stride (floats) of a warp's 16 x 8 R scratch
 
 // T Diag(beta) element pair (r, c), (r, c + 1), c even, as bf16 into the
 // K-major [T Diag(b); 0; Aqk] tile (64 token columns, one 128-byte row per r).
@@ -315,11 +315,13 @@ __device__ __forceinline__ void store_tb2(uint8_t *tbz, int r, int c, float t0, 
 
 template <int J>
 __device__ __forceinline__ void solve_block_column(const float *As, float *Ts, float *Rw, int lane,
-                                                   uint8_t *tbz, const float *beta) {
+                                                   uint8_t *tbz, const float *beta, int nt) {
+    // This warp owns the 8 columns 16J + 8nt .. +7 of block column J; the two
+    // halves of a block column never read each other's results.
     const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int I = J + 1; I < 4; ++I) {
-        float rc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float rc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int K = J; K < I; ++K) {
 #pragma unroll
@@ -328,47 +330,34 @@ __device__ __forceinline__ void solve_block_column(const float *As, float *Ts, f
                 const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * AS]), to_tf32(ar[4]),
                                        to_tf32(ar[8 * AS + 4])};
                 const int rr = 16 * K + 8 * ks + t4;   // rr % 4 == t4, also for rr + 4
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int cc = (16 * J + 8 * nt + g) ^ (t4 << 3);
-                    const uint32_t b[2] = {to_tf32(Ts[rr * 64 + cc]), to_tf32(Ts[(rr + 4) * 64 + cc])};
-                    mma_tf32(rc[nt], a, b);
-                }
+                const int cc = (16 * J + 8 * nt + g) ^ (t4 << 3);
+                const uint32_t b[2] = {to_tf32(Ts[rr * 64 + cc]), to_tf32(Ts[(rr + 4) * 64 + cc])};
+                mma_tf32(rc, a, b);
             }
         }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            Rw[g * RW + 8 * nt + 2 * t4] = rc[nt][0];
-            Rw[g * RW + 8 * nt + 2 * t4 + 1] = rc[nt][1];
-            Rw[(g + 8) * RW + 8 * nt + 2 * t4] = rc[nt][2];
-            Rw[(g + 8) * RW + 8 * nt + 2 * t4 + 1] = rc[nt][3];
-        }
+        Rw[g * RW + 2 * t4] = rc[0];
+        Rw[g * RW + 2 * t4 + 1] = rc[1];
+        Rw[(g + 8) * RW + 2 * t4] = rc[2];
+        Rw[(g + 8) * RW + 2 * t4 + 1] = rc[3];
         __syncwarp();
-        float tc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float tc[4] = {0.f, 0.f, 0.f, 0.f};
         const int sw = (g & 3) << 3;   // swizzle of rows 16I + g and 16I + g + 8
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             const int c0 = (16 * I + 8 * ks + t4) ^ sw, c1 = (16 * I + 8 * ks + t4 + 4) ^ sw;
             const uint32_t a[4] = {to_tf32(Ts[(16 * I + g) * 64 + c0]), to_tf32(Ts[(16 * I + g + 8) * 64 + c0]),
                                    to_tf32(Ts[(16 * I + g) * 64 + c1]), to_tf32(Ts[(16 * I + g + 8) * 64 + c1])};
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t b[2] = {to_tf32(Rw[(8 * ks + t4) * RW + 8 * nt + g]),
-                                       to_tf32(Rw[(8 * ks + t4 + 4) * RW + 8 * nt + g])};
-                mma_tf32(tc[nt], a, b);
-            }
+            const uint32_t b[2] = {to_tf32(Rw[(8 * ks + t4) * RW + g]), to_tf32(Rw[(8 * ks + t4 + 4) * RW + g])};
+            mma_tf32(tc, a, b);
         }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int c = (16 * J + 8 * nt + 2 * t4) ^ sw;
-            Ts[(16 * I + g) * 64 + c] = -tc[nt][0];
-            Ts[(16 * I + g) * 64 + c + 1] = -tc[nt][1];
-            Ts[(16 * I + g + 8) * 64 + c] = -tc[nt][2];
-            Ts[(16 * I + g + 8) * 64 + c + 1] = -tc[nt][3];
-            const int cl = 16 * J + 8 * nt + 2 * t4;
-            store_tb2(tbz, 16 * I + g, cl, -tc[nt][0], -tc[nt][1], beta);
-            store_tb2(tbz, 16 * I + g + 8, cl, -tc[nt][2], -tc[nt][3], beta);
-        }
+        const int cl = 16 * J + 8 * nt + 2 * t4;
+        const int c = cl ^ sw;
+        Ts[(16 * I + g) * 64 + c] = -tc[0];
+        Ts[(16 * I + g) * 64 + c + 1] = -tc[1];
+        Ts[(16 * I + g + 8) * 64 + c] = -tc[2];
+        Ts[(16 * I + g + 8) * 64 + c + 1] = -tc[3];
+        store_tb2(tbz, 16 * I + g, cl, -tc[0], -tc[1], beta);
+        store_tb2(tbz, 16 * I + g + 8, cl, -tc[2], -tc[3], beta);
         __syncwarp();
     }
 }
@@ -656,9 +645,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             }
         }
         __syncthreads();
-        if (warp == 0) solve_block_column<0>(As, Ts, Rws, lane, sm + OP_TBZ, beta_s);
-        else if (warp == 1) solve_block_column<1>(As, Ts, Rws + 16 * RW, lane, sm + OP_TBZ, beta_s);
-        else if (warp == 2) solve_block_column<2>(As, Ts, Rws + 32 * RW, lane, sm + OP_TBZ, beta_s);
+        if (warp < 2) solve_block_column<0>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
+        else if (warp < 4) solve_block_column<1>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
+        else if (warp < 6) solve_block_column<2>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
         fence_proxy_async();
         __syncthreads();
 
