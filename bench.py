@@ -210,6 +210,36 @@ def bench_varlen(args, ws, sampler):
                 h2d=h2d, d2h=d2h, launches_per_step=1)
 
 
+def bench_varlen_checkpoints(args, ws, interval=256):
+    """The varlen workload with the state also written after every 256 tokens
+    of each sequence (the prefix cache's block) into a slot list."""
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    w = varlen_workload(dev)
+    x, N, H, T = w["x"], w["N"], w["H"], w["T"]
+    lengths = list(w["lengths"])
+    cap = max(lengths) // interval
+    made = sum(min(L // interval, cap) for L in lengths)
+    pool = torch.empty(2 * N + N * cap, H, KD, VD, device=dev)
+    pool[:N] = w["ck"]
+    slots = torch.arange(2 * N, 2 * N + N * cap, dtype=torch.int32, device=dev).view(N, cap)
+    cu_d = w["cu"].to(dev)
+    init = torch.arange(N, dtype=torch.int32, device=dev)
+    out = torch.arange(N, 2 * N, dtype=torch.int32, device=dev)
+    o = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
+    cu_h = w["cu"]
+
+    def step():
+        kda.kda_chunk_prefill_checkpoints(x["q"], x["k"], x["v"], x["gk"], x["beta"], cu_d, cu_h,
+                                          pool, init, out, interval, slots, o=o)
+
+    ms = timed(step, args.steps, args.warmup, ws)
+    alg = algorithmic_prefill_bytes(T, H, N) + made * H * STATE_B
+    del pool
+    torch.cuda.empty_cache()
+    return dict(ms=ms, T=T, alg_bytes=alg, checkpoints=made, interval=interval)
+
+
 def bench_long(args, ws, N=4, T=24576, H=96, piece=4096, steps=None):
     """Six 4096-token pieces of 4 x 24576 tokens (H = 96), each piece one
     kda_chunk_prefill over the 4 sequences resuming in place from the working
@@ -384,7 +414,20 @@ class OracleVarlen:
 # main
 # ---------------------------------------------------------------------------
 
-def profile_traffic(kernel_src, summary_name, key="dram_bytes_per_launch"):
+CSRC = os.path.join(ROOT, "kda_state_gb300", "csrc")
+
+
+def source_sha1(kernel_file):
+    """First 12 hex digits of the sha1 over a kernel's source file followed by
+    the shared device header it includes (the hash the profile summaries
+    record as source_sha1)."""
+    h = hashlib.sha1()
+    for f in (kernel_file, "kda_common.cuh"):
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def profile_traffic(kernel_file, summary_name, key="dram_bytes_per_launch"):
     """DRAM bytes (read + write) from a committed ncu summary, if it was taken
     on the current kernel source (matched by hash); else None."""
     path = os.path.join(ROOT, "profiles", summary_name)
@@ -392,10 +435,9 @@ def profile_traffic(kernel_src, summary_name, key="dram_bytes_per_launch"):
         txt = open(path).read()
     except OSError:
         return None
-    h = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()[:12]
     m_h = re.search(r"source_sha1:\s*([0-9a-f]+)", txt)
     m_t = re.search(key + r":\s*([0-9.eE+]+)", txt)
-    if not m_h or not m_t or m_h.group(1) != h:
+    if not m_h or not m_t or m_h.group(1) != source_sha1(kernel_file):
         return None
     return float(m_t.group(1))
 
@@ -434,7 +476,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the decode / verify+fold runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--only", choices=["decode", "verify"], default=None,
+    ap.add_argument("--only", choices=["decode", "verify", "checkpoints"], default=None,
                     help="run one of the secondary workloads alone (for profiling)")
     ap.add_argument("--layers", type=int, default=69,
                     help="layers of the --only workload (a smaller case for profiling)")
@@ -447,8 +489,11 @@ def main():
         torch.cuda.set_device(local)
         from kda_state_gb300 import _build
         _build.build()
-        fn = bench_decode if args.only == "decode" else bench_verify_fold
-        r = fn(args, 1, layers=args.layers, steps=args.steps)
+        if args.only == "checkpoints":
+            r = bench_varlen_checkpoints(args, 1)
+        else:
+            fn = bench_decode if args.only == "decode" else bench_verify_fold
+            r = fn(args, 1, layers=args.layers, steps=args.steps)
         print(json.dumps({"only": args.only, **{k: v for k, v in r.items()
                                                  if isinstance(v, (int, float))}}), flush=True)
         return
@@ -489,8 +534,7 @@ def main():
     ms = res["ms"]
     value = res["T"] / (ms / 1e3) * ws
     achieved = res["alg_bytes"] / (ms / 1e3) / 1e9
-    src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_prefill_tc.cu")
-    traffic = profile_traffic(src, "prefill_tc_kernel.varlen.md")
+    traffic = profile_traffic("kda_prefill_tc.cu", "prefill_tc_kernel.varlen.md")
     line = {
         "metric": "KDA prefill tok/s (varlen chunked prefill)",
         "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -511,8 +555,21 @@ def main():
         "cpu_baseline": cpu,
     }
     if not args.no_also:
-        rec_src = os.path.join(ROOT, "kda_state_gb300", "csrc", "kda_recurrent.cu")
         also = {}
+        try:
+            c = bench_varlen_checkpoints(args, ws)
+            also["varlen_checkpoints"] = {
+                "tok_per_s": c["T"] / (c["ms"] / 1e3) * ws, "ms_per_step": c["ms"],
+                "workload": "the varlen batch above with the state written every %d tokens "
+                            "(%d checkpoints per head) into a slot list"
+                            % (c["interval"], c["checkpoints"]),
+                "GBps": c["alg_bytes"] / (c["ms"] / 1e3) / 1e9,
+                "frac": c["alg_bytes"] / (c["ms"] / 1e3) / 1e9 / hbm,
+                "time_vs_plain": c["ms"] / res["ms"],
+                "traffic": profile_traffic("kda_prefill_tc.cu", "prefill_tc_kernel.varlen_checkpoints.md"),
+            }
+        except Exception as e:  # noqa: BLE001
+            also["varlen_checkpoints"] = {"error": repr(e)}
         try:
             lg = bench_long(args, ws)
             also["long_prefill"] = {
@@ -534,7 +591,7 @@ def main():
                 "decode_kernel_us": d["dec_ms"] * 1e3,
                 "decode_kernel_GBps": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9,
                 "decode_kernel_frac": d["dec_bytes"] / (d["dec_ms"] / 1e3) / 1e9 / hbm,
-                "decode_kernel_traffic": profile_traffic(rec_src, "decode_kernel.decode.md"),
+                "decode_kernel_traffic": profile_traffic("kda_decode.cu", "decode_kernel.decode.md"),
                 "step_GBps": (d["dec_bytes"] + d["cow_bytes"]) * d["layers"] / (d["ms"] / 1e3) / 1e9,
             }
         except Exception as e:  # noqa: BLE001
@@ -549,11 +606,11 @@ def main():
                 "verify_kernel_us": v["ver_ms"] * 1e3,
                 "verify_kernel_GBps": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9,
                 "verify_kernel_frac": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9 / hbm,
-                "verify_kernel_traffic": profile_traffic(
-                    rec_src, "verify_block_kernel_fold_kernel.verify.md", "verify_dram_bytes_per_launch"),
+                "verify_kernel_traffic": profile_traffic("kda_verify.cu", "verify_block_kernel.verify.md"),
                 "fold_kernel_us": v["fold_ms"] * 1e3,
                 "fold_kernel_GBps": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9,
                 "fold_kernel_frac": v["fold_bytes"] / (v["fold_ms"] / 1e3) / 1e9 / hbm,
+                "fold_kernel_traffic": profile_traffic("kda_fold.cu", "fold_kernel.verify.md"),
             }
         except Exception as e:  # noqa: BLE001
             also["verify_fold"] = {"error": repr(e)}

@@ -154,6 +154,39 @@ KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int 
                               void *stream);
 
 /*
+ * kda_chunk_prefill_checkpoints -- kda_chunk_prefill that also writes the
+ * state at every ckpt_interval tokens of each sequence.
+ *
+ * Prefix caching keeps exact states only at fixed token boundaries: the Kimi
+ * K3 on B200 deployment notes (item "CuTe FlashKDA prefill") cut every
+ * non-last chunk to a multiple of the cache's 256-token block so that the
+ * kernel's end-of-chunk state is an exact checkpoint, and "SGLang and Miles Add
+ * Day-0 Support for Kimi K3", section "Prefix caching for a recurrent state",
+ * keeps such checkpoints sparsely on the radix tree.  This call emits every
+ * one of a sequence's boundary states from the same launch as its prefill.
+ *
+ *   (all arguments of kda_chunk_prefill, same meaning)
+ *   ckpt_interval  tokens between checkpoints, a positive multiple of 64
+ *   ckpt_slots     device int32 [N][max_ckpts]: checkpoint m of sequence n (the
+ *                  state after (m + 1) * ckpt_interval of its tokens in this
+ *                  call) goes to slot ckpt_slots[n * max_ckpts + m]; -1 skips it;
+ *                  checkpoints past max_ckpts or past the sequence are not made
+ *   max_ckpts      >= 1
+ * A checkpoint equals, bit for bit, the final state of the same call made on
+ * the sequence's first (m + 1) * ckpt_interval tokens.
+ */
+KDA_API int kda_chunk_prefill_checkpoints(kda_dtype dt, int num_seqs, int total_tokens, int H,
+                                          int K, int V, const void *q, const void *k,
+                                          const void *v, const void *gk, const void *beta,
+                                          const int32_t *cu_seqlens_dev,
+                                          const int32_t *cu_seqlens_host, float *state_pool,
+                                          int num_slots, const int32_t *init_slot,
+                                          const int32_t *out_slot, const int32_t *snap_slot,
+                                          int ckpt_interval, const int32_t *ckpt_slots,
+                                          int max_ckpts, void *o, float scale, int32_t *dev_err,
+                                          void *stream);
+
+/*
  * kda_decode_step -- one token per request, state updated in place.
  *
  * The working slot is read and overwritten by every forward ("SGLang and Miles

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     KdaError,
     RingBuffers,
     kda_chunk_prefill,
+    kda_chunk_prefill_checkpoints,
     kda_decode_step,
     kda_replay_fold,
     kda_ring,

@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f, ip = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
         L.kda_chunk_prefill.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, ip, vp, i, ip, ip,
                                         ip, vp, f, ip, vp]
+        L.kda_chunk_prefill_checkpoints.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, ip,
+                                                    vp, i, ip, ip, ip, i, ip, i, vp, f, ip, vp]
         L.kda_decode_step.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i, vp, f, ip, vp]
         L.kda_verify_store_inputs.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i,
                                               ctypes.POINTER(kda_ring), ip, vp, f, ip, vp]
@@ -65,7 +67,7 @@ def lib() -> ctypes.CDLL:
                                       ctypes.POINTER(kda_ring), i, i, ip, ip, ip, ip, vp]
         L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
                                     i, ip, vp]
-        for fn in ("kda_chunk_prefill", "kda_decode_step", "kda_verify_store_inputs",
+        for fn in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step", "kda_verify_store_inputs",
                    "kda_replay_fold", "kda_slot_copy"):
             getattr(L, fn).restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -174,6 +176,30 @@ def kda_chunk_prefill(q, k, v, gk, beta, cu_seqlens, cu_seqlens_host, state_pool
         _dt(q), N, T, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(cu_seqlens), hp,
         _p(state_pool), state_pool.shape[0], _p(init_slot), _p(out_slot), _p(snap_slot), _p(o),
         float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
+def kda_chunk_prefill_checkpoints(q, k, v, gk, beta, cu_seqlens, cu_seqlens_host, state_pool,
+                                  init_slot, out_slot, ckpt_interval: int, ckpt_slots,
+                                  snap_slot=None, o=None, scale: float = 1.0, dev_err=None,
+                                  stream=None):
+    """``kda_chunk_prefill`` that also writes the state after every
+    ``ckpt_interval`` tokens of sequence n into slot ``ckpt_slots[n, m]``
+    (int32 [N, max_ckpts] on the device, -1 skips).  Returns o."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    N = host.numel() - 1
+    if ckpt_slots.dim() != 2 or ckpt_slots.shape[0] != N or not ckpt_slots.is_contiguous():
+        raise ValueError("ckpt_slots must be a contiguous int32 [N, max_ckpts] tensor")
+    if o is None:
+        o = torch.empty(T, H, V, dtype=q.dtype, device=q.device)
+    hp = host.numpy().ctypes.data_as(ctypes.c_void_p)
+    _check("kda_chunk_prefill_checkpoints", lib().kda_chunk_prefill_checkpoints(
+        _dt(q), N, T, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(cu_seqlens), hp,
+        _p(state_pool), state_pool.shape[0], _p(init_slot), _p(out_slot), _p(snap_slot),
+        int(ckpt_interval), _p(ckpt_slots), ckpt_slots.shape[1], _p(o), float(scale),
+        _p(dev_err), _stream(stream)))
     return o
 
 

@@ -27,13 +27,13 @@ KDA_API const char *kda_status_string(int status) {
     }
 }
 
-KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
-                              const void *q, const void *k, const void *v, const void *gk,
-                              const void *beta, const int32_t *cu_seqlens_dev,
-                              const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
-                              const int32_t *init_slot, const int32_t *out_slot,
-                              const int32_t *snap_slot, void *o, float scale, int32_t *dev_err,
-                              void *stream) {
+static int prefill_impl(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
+                        const void *q, const void *k, const void *v, const void *gk,
+                        const void *beta, const int32_t *cu_seqlens_dev,
+                        const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
+                        const int32_t *init_slot, const int32_t *out_slot,
+                        const int32_t *snap_slot, int ckpt_interval, const int32_t *ckpt_slots,
+                        int max_ckpts, void *o, float scale, int32_t *dev_err, void *stream) {
     if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
     if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || num_slots < 1 || !isfinite(scale))
@@ -55,6 +55,7 @@ KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int 
     a.cu = cu_seqlens_dev; a.cu_host = cu_seqlens_host;
     a.pool = state_pool; a.init_slot = init_slot; a.out_slot = out_slot; a.snap_slot = snap_slot;
     a.o = o; a.scale = scale; a.err = dev_err;
+    a.ckpt_interval = ckpt_interval; a.max_ckpts = max_ckpts; a.ckpt_slots = ckpt_slots;
     cudaStream_t s = (cudaStream_t)stream;
     if (dt == KDA_DTYPE_BF16) {
         // the tensor-core kernel stages q, k, v, gk with TMA and stores o in 16-byte vectors
@@ -64,6 +65,36 @@ KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int 
         return from_cuda(kda::launch_prefill_chunked(a, s));
     }
     return from_cuda(kda::launch_prefill_recurrent(a, s));
+}
+
+KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
+                              const void *q, const void *k, const void *v, const void *gk,
+                              const void *beta, const int32_t *cu_seqlens_dev,
+                              const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
+                              const int32_t *init_slot, const int32_t *out_slot,
+                              const int32_t *snap_slot, void *o, float scale, int32_t *dev_err,
+                              void *stream) {
+    return prefill_impl(dt, num_seqs, total_tokens, H, K, V, q, k, v, gk, beta, cu_seqlens_dev,
+                        cu_seqlens_host, state_pool, num_slots, init_slot, out_slot, snap_slot,
+                        0, nullptr, 0, o, scale, dev_err, stream);
+}
+
+KDA_API int kda_chunk_prefill_checkpoints(kda_dtype dt, int num_seqs, int total_tokens, int H,
+                                          int K, int V, const void *q, const void *k,
+                                          const void *v, const void *gk, const void *beta,
+                                          const int32_t *cu_seqlens_dev,
+                                          const int32_t *cu_seqlens_host, float *state_pool,
+                                          int num_slots, const int32_t *init_slot,
+                                          const int32_t *out_slot, const int32_t *snap_slot,
+                                          int ckpt_interval, const int32_t *ckpt_slots,
+                                          int max_ckpts, void *o, float scale, int32_t *dev_err,
+                                          void *stream) {
+    if (ckpt_interval < 64 || ckpt_interval % 64 != 0 || max_ckpts < 1 || !ckpt_slots)
+        return KDA_ERR_INVALID_ARG;
+    if ((long long)num_seqs * max_ckpts > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    return prefill_impl(dt, num_seqs, total_tokens, H, K, V, q, k, v, gk, beta, cu_seqlens_dev,
+                        cu_seqlens_host, state_pool, num_slots, init_slot, out_slot, snap_slot,
+                        ckpt_interval, ckpt_slots, max_ckpts, o, scale, dev_err, stream);
 }
 
 KDA_API int kda_decode_step(kda_dtype dt, int B, int H, int K, int V, const void *q,

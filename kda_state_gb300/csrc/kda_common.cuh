@@ -42,6 +42,24 @@ __device__ __forceinline__ void report(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
+// Checkpoints a prefill unit of len tokens makes: one after every interval
+// tokens, at most max_ckpts (interval 0: none).
+__device__ __forceinline__ int ckpt_count(int len, int interval, int max_ckpts) {
+    return interval > 0 ? min(len / interval, max_ckpts) : 0;
+}
+
+// Block-wide check that every checkpoint slot sequence n will use lies in
+// [-1, num_slots).  Every thread of the block must call it.
+__device__ __forceinline__ bool ckpt_slots_ok(const int32_t *slots, int n, int count,
+                                              int max_ckpts, int num_slots) {
+    int bad = 0;
+    for (int m = threadIdx.x; m < count; m += blockDim.x) {
+        const int s = slots[(size_t)n * max_ckpts + m];
+        bad |= s < -1 || s >= num_slots;
+    }
+    return !__syncthreads_or(bad);
+}
+
 // fp32 -> tf32 bit pattern, round to nearest.
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
     uint32_t r;
@@ -216,6 +234,13 @@ __device__ __forceinline__ float token_update(StateRegs &r, const TokenIn &in, R
         r.s[i] = s;
     }
     return o;
+}
+
+// Opt a kernel into more than 48 KB of dynamic shared memory when it needs it.
+template <typename Kernel>
+cudaError_t set_smem(Kernel kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 }  // namespace kda

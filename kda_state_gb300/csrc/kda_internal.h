@@ -64,6 +64,9 @@ struct PrefillArgs {
     void *o;
     float scale;
     int32_t *err;
+    int ckpt_interval;             // 0: no checkpoints
+    int max_ckpts;
+    const int32_t *ckpt_slots;     // device [N][max_ckpts]
 };
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);

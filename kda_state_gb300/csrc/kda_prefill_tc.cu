@@ -108,6 +108,8 @@ struct Params {
     __nv_bfloat16 *o;
     float scale;
     int32_t *err;
+    int ckpt_chunks, max_ckpts;     // checkpoint every ckpt_chunks chunks (0: none)
+    const int32_t *ckpt_slots;
     int32_t order[KDA_MAX_LPT_SEQS];
 };
 
@@ -392,7 +394,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     }
     const int si = p.init_slot[n], so = p.out_slot[n];
     const int ss = p.snap_slot ? p.snap_slot[n] : -1;
-    if (si < -1 || si >= p.num_slots || so < 0 || so >= p.num_slots || ss >= p.num_slots) {
+    const int nck = ckpt_count(eos - bos, p.ckpt_chunks * C, p.max_ckpts);
+    if (si < -1 || si >= p.num_slots || so < 0 || so >= p.num_slots || ss >= p.num_slots ||
+        !ckpt_slots_ok(p.ckpt_slots, n, nck, p.max_ckpts, p.num_slots)) {
         if (tid == 0 && h == 0) report(p.err, DEVERR_SLOT_RANGE);
         return;
     }
@@ -756,6 +760,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 store_f16(sm, OP_S + chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
+            // the exact state after (m + 1) * ckpt_chunks full chunks
+            const int m = (c + 1) / max(p.ckpt_chunks, 1) - 1;
+            if (nck > 0 && (c + 1) % p.ckpt_chunks == 0 && m < nck && !(*flags & FLAG_TIMEOUT)) {
+                const int cs = p.ckpt_slots[(size_t)n * p.max_ckpts + m];
+                if (cs >= 0) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        p.pool + ((size_t)cs * p.H + h) * STATE_ELEMS + (size_t)srow * VD + 32 * cq);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcs(dst + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
+                }
+            }
         }
         // No block barrier here: each warp goes on to the next chunk's loads
         // and scan.  The next chunk's first barrier orders these TMEM reads
@@ -843,6 +859,7 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
     p.beta = (const __nv_bfloat16 *)a.beta; p.cu = a.cu; p.pool = a.pool;
     p.init_slot = a.init_slot; p.out_slot = a.out_slot; p.snap_slot = a.snap_slot;
     p.o = (__nv_bfloat16 *)a.o; p.scale = a.scale; p.err = a.err;
+    p.ckpt_chunks = a.ckpt_interval / C; p.max_ckpts = a.max_ckpts; p.ckpt_slots = a.ckpt_slots;
     p.lpt = a.N <= KDA_MAX_LPT_SEQS;
     if (p.lpt) {
         std::vector<int> idx(a.N);

@@ -79,7 +79,7 @@ def load_variant(src_path: str, out_path: str):
     lib = _bind(build(force=True, src=src_path, out=out_path))
     import types
     ns = types.SimpleNamespace()
-    for name in ("unit", "prefill_varlen", "decode", "verify", "fold"):
+    for name in ("unit", "prefill_varlen", "prefill_checkpoints", "decode", "verify", "fold"):
         fn = globals()[name]
         ns.__dict__[name] = (lambda f: (lambda *a, **kw: f(*a, _lib=lib, **kw)))(fn)
     return ns
@@ -166,6 +166,56 @@ def prefill_varlen(q, k, v, gk, beta, cu_seqlens, S0, scale: float = 1.0, chunk:
     for i, (n, h) in enumerate(units):
         Sout[n, h] = S[i]
     return o, Sout
+
+
+def prefill_checkpoints(q, k, v, gk, beta, cu_seqlens, S0, interval: int, max_ckpts: int,
+                        scale: float = 1.0, nthreads: int = 0, heads=None, seqs=None, _lib=None):
+    """Varlen prefill that also returns the state after every ``interval``
+    tokens of each sequence: checkpoint m of sequence n is the state once the
+    recurrence has taken the sequence's first (m + 1) * interval tokens.
+
+    Prefix caching keeps states only at fixed token boundaries (Kimi K3 on B200
+    deployment notes, item "CuTe FlashKDA prefill": non-last chunks cut to
+    multiples of the 256-token cache block so that the end-of-chunk state is an
+    exact checkpoint).  Each sequence is run as consecutive pieces of
+    ``interval`` tokens, each piece starting from the state the previous one
+    left, and the state is read after every full piece.
+
+    Returns (o [T, H, V], S [N, H, K, V], ckpt [N, max_ckpts, H, K, V],
+    made [N]); checkpoints a sequence does not reach stay zero and made[n]
+    counts the ones it does (at most max_ckpts)."""
+    q, k, v, gk, beta = (_f64(x) for x in (q, k, v, gk, beta))
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    H = q.shape[1]
+    S0 = _f64(S0)
+    seqs = list(range(N)) if seqs is None else list(seqs)
+    heads = list(range(H)) if heads is None else list(heads)
+    units = [(n, h) for n in seqs for h in heads]
+    lens = np.array([cu[n + 1] - cu[n] for n, _ in units], dtype=np.int64)
+    S = np.stack([S0[n, h] for n, h in units]) if units else np.zeros((0,) + S0.shape[2:])
+    S = np.ascontiguousarray(S)
+    o = np.zeros(v.shape, np.float64)
+    ckpt = np.zeros((N, max_ckpts, H) + S0.shape[2:], np.float64)
+    made = np.zeros(N, np.int64)
+    for n in seqs:
+        made[n] = min((cu[n + 1] - cu[n]) // interval, max_ckpts)
+    start = 0
+    while units and start < lens.max():
+        piece = np.clip(lens - start, 0, interval)
+        op, _ = _batch([cu[n] + start for n, _ in units], piece, [h for _, h in units],
+                       q, k, v, gk, beta, S, scale, True, 0, nthreads, _lib)
+        for i, (n, h) in enumerate(units):
+            sl = slice(cu[n] + start, cu[n] + start + piece[i])
+            o[sl, h] = op[sl, h]
+            m = start // interval
+            if piece[i] == interval and m < max_ckpts:
+                ckpt[n, m, h] = S[i]
+        start += interval
+    Sout = S0.copy()
+    for i, (n, h) in enumerate(units):
+        Sout[n, h] = S[i]
+    return o, Sout, ckpt, made
 
 
 def decode(q, k, v, gk, beta, S0, scale: float = 1.0, nthreads: int = 0, _lib=None):

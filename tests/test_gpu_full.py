@@ -58,6 +58,59 @@ def test_varlen_prefill_full(init):
     assert_close(pool[N:, heads], S_ref, torch.bfloat16, "final states")
 
 
+def test_varlen_prefill_checkpoints_full():
+    """The varlen workload with a checkpoint every 256 tokens (the prefix
+    cache's block), launched as the benchmark launches it: outputs and final
+    states bit-identical to the plain prefill; every checkpoint bit-identical
+    to the final state of a plain prefill of that prefix; three heads of every
+    sequence vs the oracle."""
+    w = gen.varlen_batch(DEV)
+    x, N, H, cu = w["x"], w["N"], w["H"], w["cu"]
+    I = 256
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    cap = max(lengths) // I
+    made = [L // I for L in lengths]
+    slots = torch.arange(2 * N, 2 * N + N * cap, dtype=torch.int32).view(N, cap)
+    pool = torch.zeros(2 * N + N * cap, H, KD, VD, device=DEV)
+    pool[:N] = w["ck"]
+    init = torch.arange(N, dtype=torch.int32, device=DEV)
+    out = torch.arange(N, 2 * N, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = kda().kda_chunk_prefill_checkpoints(x["q"], x["k"], x["v"], x["gk"], x["beta"],
+                                            cu.to(DEV), cu, pool, init, out, I, slots.to(DEV),
+                                            dev_err=err)
+    pool_p = torch.zeros(2 * N, H, KD, VD, device=DEV)
+    pool_p[:N] = w["ck"]
+    o_p = kda().kda_chunk_prefill(x["q"], x["k"], x["v"], x["gk"], x["beta"], cu.to(DEV), cu,
+                                  pool_p, init, out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o, o_p) and torch.equal(pool[N:2 * N], pool_p[N:])
+    offs = cu.tolist()
+    for m in range(cap):
+        keep = [min(L, (m + 1) * I) for L in lengths]
+        idx = torch.cat([torch.arange(offs[n], offs[n] + keep[n]) for n in range(N)]).to(DEV)
+        xp = {k_: t.index_select(0, idx).contiguous() for k_, t in x.items()}
+        cup = gen.cu_seqlens(keep)
+        pool_q = pool_p.clone()
+        pool_q[:N] = w["ck"]
+        kda().kda_chunk_prefill(xp["q"], xp["k"], xp["v"], xp["gk"], xp["beta"], cup.to(DEV), cup,
+                                pool_q, init, out)
+        torch.cuda.synchronize()
+        for n in range(N):
+            if m < made[n]:
+                assert torch.equal(pool[int(slots[n, m])], pool_q[N + n]), (m, n)
+    heads = [0, 29, 63]
+    xs = _host(x, heads)
+    _, _, ck_ref, made_ref = oracle.prefill_checkpoints(
+        xs["q"], xs["k"], xs["v"], xs["gk"], xs["beta"], cu.numpy(), f64(w["ck"][:, heads]), I, cap)
+    assert list(made_ref) == made
+    for n in range(N):
+        for m in range(made[n]):
+            assert_close(pool[int(slots[n, m])][heads], ck_ref[n, m], torch.bfloat16,
+                         "checkpoint %d of sequence %d" % (m, n))
+
+
 def test_long_prefill_pieces_full():
     """4 sequences x 24576 tokens, H = 96, bf16, from checkpoints, as six
     pieces of 4096 tokens that resume in place; after each piece the state is

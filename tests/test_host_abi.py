@@ -27,8 +27,8 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     names = declared_symbols()
-    for n in ("kda_chunk_prefill", "kda_decode_step", "kda_verify_store_inputs",
-              "kda_replay_fold", "kda_slot_copy", "kda_status_string"):
+    for n in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step",
+              "kda_verify_store_inputs", "kda_replay_fold", "kda_slot_copy", "kda_status_string"):
         assert n in names
 
 
@@ -85,6 +85,21 @@ def test_prefill_rejects_bad_cu_seqlens(L):
                                FAKE, FAKE, None, None, 1.0, None, None)) == 0
     assert L.kda_chunk_prefill(*(0, 1, 4, 2, 128, 96) + (FAKE,) * 6 + (_cu([0, 4]), FAKE, 4,
                                FAKE, FAKE, None, FAKE, 1.0, None, None)) == -2
+
+
+def test_prefill_checkpoints_rejects(L):
+    def args(interval, slots, max_ckpts, cu=None, N=2, T=9):
+        return (0, N, T, 2, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                cu if cu is not None else _cu([0, 5, 9]), FAKE, 4, FAKE, FAKE, None, interval,
+                slots, max_ckpts, FAKE, 1.0, None, None)
+    assert L.kda_chunk_prefill_checkpoints(*args(0, FAKE, 1)) == -1      # no interval
+    assert L.kda_chunk_prefill_checkpoints(*args(100, FAKE, 1)) == -1    # not a multiple of 64
+    assert L.kda_chunk_prefill_checkpoints(*args(-64, FAKE, 1)) == -1
+    assert L.kda_chunk_prefill_checkpoints(*args(256, None, 1)) == -1    # no slot list
+    assert L.kda_chunk_prefill_checkpoints(*args(256, FAKE, 0)) == -1    # max_ckpts < 1
+    # the plain prefill's own checks still apply
+    assert L.kda_chunk_prefill_checkpoints(*args(256, FAKE, 2, _cu([0, 5, 3]), 2, 3)) == -1
+    assert L.kda_chunk_prefill_checkpoints(*args(256, FAKE, 2, _cu([0]), 0, 0)) == 0
 
 
 def test_verify_and_fold_ring_rules(L):

@@ -223,6 +223,42 @@ def pin_batches_equal_units(orc):
             assert np.array_equal(Sd[b, h], Su)
 
 
+def pin_checkpoints_are_prefix_states(orc):
+    """Checkpoint m of a sequence is the state after its first (m + 1) * I
+    tokens: written out as a brute-force product of the definition's per-token
+    matrices on tiny sizes, for sequences that end on, before and between
+    boundaries, with a cap on the number kept; the outputs and final states
+    are those of the plain varlen run."""
+    rng = _rng(13)
+    H, K, V, I, cap = 2, 4, 3, 4, 2
+    lens = [9, 3, 8, 12, 0]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    q = rng.standard_normal((T, H, K))
+    k = rng.standard_normal((T, H, K))
+    v = rng.standard_normal((T, H, V))
+    gk = -rng.uniform(0, 1, (T, H, K))
+    beta = rng.uniform(0, 1, (T, H))
+    S0 = rng.standard_normal((len(lens), H, K, V))
+    o, S, ck, made = orc.prefill_checkpoints(q, k, v, gk, beta, cu, S0, I, cap, scale=0.6)
+    assert list(made) == [2, 0, 2, 2, 0]
+    for n, L in enumerate(lens):
+        for h in range(H):
+            St = S0[n, h].copy()
+            kept = []
+            for t in range(cu[n], cu[n + 1]):
+                P = np.eye(K) - beta[t, h] * np.outer(k[t, h], k[t, h])
+                St = P @ np.diag(np.exp(gk[t, h])) @ St + beta[t, h] * np.outer(k[t, h], v[t, h])
+                if (t - cu[n] + 1) % I == 0:
+                    kept.append(St.copy())
+            for m in range(cap):
+                want = kept[m] if m < len(kept) else np.zeros((K, V))
+                np.testing.assert_allclose(ck[n, m, h], want, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(S[n, h], St, rtol=1e-12, atol=1e-13)
+    o2, S2 = orc.prefill_varlen(q, k, v, gk, beta, cu, S0, scale=0.6)
+    assert np.array_equal(o, o2) and np.array_equal(S, S2)
+
+
 PINS = [
     pin_single_token_closed_form,
     pin_identity_when_no_write_no_decay,
@@ -235,6 +271,7 @@ PINS = [
     pin_chunked_equals_sequential,
     pin_fold_is_prefix_commit,
     pin_batches_equal_units,
+    pin_checkpoints_are_prefix_states,
 ]
 
 
