@@ -319,18 +319,30 @@ def bench_decode(args, ws, layers=69, B=384, H=64, slots=512, cow_frac=0.10, ste
                 layers=layers, n_cow=n_cow)
 
 
-def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, steps=None):
+def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, steps=None,
+                      ragged=False):
+    """Verify of B requests x G drafts on every layer, then one fold.  ragged:
+    each request verifies its own G_b <= G drafts (uniform on 1..G, packed by
+    cu_drafts) and accepts at most G_b."""
     import kda_state_gb300 as kda
     dev = "cuda"
     g = gen.make_gen(4)
     ids = gen.slot_permutation(slots, g)[:B].to(dev)
     accept = gen.accept_lengths(B, G, 0.64, g)
+    Gb = gen.draft_lengths(B, G, g) if ragged else torch.full((B,), G, dtype=torch.int32)
+    accept = torch.minimum(accept, Gb)
     acc_d = accept.to(dev)
+    cu_d = torch.cat([torch.zeros(1, dtype=torch.int32), Gb.cumsum(0).to(torch.int32)]).to(dev)
+    n_tok = int(Gb.sum())
     gd = gen.make_gen(1004, dev)
     pools = [gen.checkpoint((slots, H, KD, VD), gd, device=dev) for _ in range(layers)]
     rings = [kda.make_ring(slots, R, H, torch.bfloat16, dev) for _ in range(layers)]
-    xs = [gen.token_inputs(G, H, torch.bfloat16, gd, device=dev, lead=(B,)) for _ in range(layers)]
-    o = torch.empty(B, G, H, VD, dtype=torch.bfloat16, device=dev)
+    if ragged:
+        xs = [gen.token_inputs(n_tok, H, torch.bfloat16, gd, device=dev) for _ in range(layers)]
+        o = torch.empty(n_tok, H, VD, dtype=torch.bfloat16, device=dev)
+    else:
+        xs = [gen.token_inputs(G, H, torch.bfloat16, gd, device=dev, lead=(B,)) for _ in range(layers)]
+        o = torch.empty(B, G, H, VD, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     ev_v = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(layers)]
@@ -342,8 +354,12 @@ def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, ste
             x = xs[l]
             if record["on"]:
                 ev_v[l][0].record(stream)
-            kda.kda_verify_store_inputs(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids, pools[l],
-                                        rings[l], o=o)
+            if ragged:
+                kda.kda_verify_store_inputs_ragged(x["q"], x["k"], x["v"], x["gk"], x["beta"], cu_d,
+                                                   G, ids, pools[l], rings[l], o=o)
+            else:
+                kda.kda_verify_store_inputs(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids,
+                                            pools[l], rings[l], o=o)
             if record["on"]:
                 ev_v[l][1].record(stream)
         if record["on"]:
@@ -361,13 +377,85 @@ def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, ste
     ver_ms = statistics.median(a.elapsed_time(b) for a, b in ev_v)
     fold_ms = ev_f[0].elapsed_time(ev_f[1])
     rec = 2 * KD + 2 * VD + 4 * KD + 4
-    ver_bytes = B * H * (STATE_B + G * (3 * KD * 2 + VD * 2 + 2) + G * VD * 2 + G * rec)
+    n_units = int((Gb > 0).sum())
+    ver_bytes = H * (n_units * STATE_B + n_tok * (3 * KD * 2 + VD * 2 + 2 + VD * 2 + rec))
     acc_sum = int(accept.sum())
     fold_bytes = layers * H * (2 * STATE_B * int((accept > 0).sum()) + acc_sum * rec)
     del pools, rings, xs
     torch.cuda.empty_cache()
     return dict(ms=ms, ver_ms=ver_ms, fold_ms=fold_ms, ver_bytes=ver_bytes, fold_bytes=fold_bytes,
-                accepted=acc_sum, mean_accept=acc_sum / B, B=B, G=G, layers=layers, H=H)
+                accepted=acc_sum, mean_accept=acc_sum / B, B=B, G=G, layers=layers, H=H,
+                verified=n_tok, mean_draft=n_tok / B)
+
+
+def bench_snapshot_ab(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, steps=None):
+    """A/B of the two ways to make speculation reversible, on one workload:
+    ReplaySSM (verify storing ~1 KB records, then one fold) against the
+    snapshot-per-step baseline (verify writing the 64 KB state after every
+    draft step, then one commit copy).  Same drafts, pools and accept lengths."""
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    g = gen.make_gen(4)
+    ids = gen.slot_permutation(slots, g)[:B].to(dev)
+    acc_d = gen.accept_lengths(B, G, 0.64, g).to(dev)
+    snap_ids = torch.arange(B, dtype=torch.int32, device=dev)
+    gd = gen.make_gen(1004, dev)
+    pools = [gen.checkpoint((slots, H, KD, VD), gd, device=dev) for _ in range(layers)]
+    rings = [kda.make_ring(slots, R, H, torch.bfloat16, dev) for _ in range(layers)]
+    snaps = [torch.empty(B, G, H, KD, VD, device=dev) for _ in range(layers)]
+    xs = [gen.token_inputs(G, H, torch.bfloat16, gd, device=dev, lead=(B,)) for _ in range(layers)]
+    o = torch.empty(B, G, H, VD, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(layers)] for k in ("ver", "snap")}
+    ev1 = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for k in ("fold", "commit")}
+    record = {"on": False}
+
+    def mark(pair, i):
+        if record["on"]:
+            pair[i].record(stream)
+
+    def step_replay():
+        for l in range(layers):
+            x = xs[l]
+            mark(ev["ver"][l], 0)
+            kda.kda_verify_store_inputs(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids, pools[l],
+                                        rings[l], o=o)
+            mark(ev["ver"][l], 1)
+        mark(ev1["fold"], 0)
+        kda.kda_replay_fold(pools, rings, ids, acc_d, max_accept=G)
+        mark(ev1["fold"], 1)
+
+    def step_snap():
+        for l in range(layers):
+            x = xs[l]
+            mark(ev["snap"][l], 0)
+            kda.kda_verify_snapshot(x["q"], x["k"], x["v"], x["gk"], x["beta"], ids, pools[l],
+                                    snaps[l], snap_ids, o=o)
+            mark(ev["snap"][l], 1)
+        mark(ev1["commit"], 0)
+        kda.kda_snapshot_commit(pools, snaps, ids, snap_ids, acc_d)
+        mark(ev1["commit"], 1)
+
+    K = steps or max(3, min(args.steps, 10))
+    res = {}
+    for name, fn in (("replayssm", step_replay), ("snapshot", step_snap)):
+        ms = timed(fn, K, 3, ws)
+        record["on"] = True
+        fn()
+        torch.cuda.synchronize()
+        record["on"] = False
+        vk, ck = ("ver", "fold") if name == "replayssm" else ("snap", "commit")
+        res[name] = {"ms_per_step": ms,
+                     "verify_kernel_us": statistics.median(a.elapsed_time(b) for a, b in ev[vk]) * 1e3,
+                     "commit_kernel_us": ev1[ck][0].elapsed_time(ev1[ck][1]) * 1e3}
+    rec = 2 * KD * 2 + 4 * KD + 4
+    res["replayssm"]["draft_bytes_per_request"] = layers * H * R * rec
+    res["snapshot"]["draft_bytes_per_request"] = layers * H * G * STATE_B
+    del pools, rings, snaps, xs
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -476,7 +564,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the decode / verify+fold runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--only", choices=["decode", "verify", "checkpoints"], default=None,
+    ap.add_argument("--only", choices=["decode", "verify", "verify_ragged", "snapshot_ab",
+                                       "checkpoints"],
+                    default=None,
                     help="run one of the secondary workloads alone (for profiling)")
     ap.add_argument("--layers", type=int, default=69,
                     help="layers of the --only workload (a smaller case for profiling)")
@@ -491,6 +581,11 @@ def main():
         _build.build()
         if args.only == "checkpoints":
             r = bench_varlen_checkpoints(args, 1)
+        elif args.only == "snapshot_ab":
+            r = bench_snapshot_ab(args, 1, layers=args.layers, steps=args.steps)
+            r = {f"{a}_{k}": v for a, d in r.items() for k, v in d.items()}
+        elif args.only == "verify_ragged":
+            r = bench_verify_fold(args, 1, layers=args.layers, steps=args.steps, ragged=True)
         else:
             fn = bench_decode if args.only == "decode" else bench_verify_fold
             r = fn(args, 1, layers=args.layers, steps=args.steps)
@@ -614,6 +709,31 @@ def main():
             }
         except Exception as e:  # noqa: BLE001
             also["verify_fold"] = {"error": repr(e)}
+        try:
+            ab = bench_snapshot_ab(args, ws)
+            ab["workload"] = ("64 req x 8 draft tok, 69 layers, H=64, 128-slot pools: ReplaySSM "
+                              "(records + fold) vs snapshot per draft step (+ commit copy)")
+            ab["draft_memory_ratio"] = (ab["snapshot"]["draft_bytes_per_request"]
+                                        / ab["replayssm"]["draft_bytes_per_request"])
+            also["snapshot_ab"] = ab
+        except Exception as e:  # noqa: BLE001
+            also["snapshot_ab"] = {"error": repr(e)}
+        try:
+            v = bench_verify_fold(args, ws, ragged=True)
+            also["verify_fold_ragged"] = {
+                "accepted_tok_per_s": v["accepted"] / (v["ms"] / 1e3) * ws,
+                "verified_tok_per_s": v["verified"] / (v["ms"] / 1e3) * ws,
+                "ms_per_step": v["ms"], "mean_accept": v["mean_accept"],
+                "mean_draft": v["mean_draft"],
+                "workload": "64 req x G_b ~ U{1..8} draft tok (trimmed windows), 69 layers, H=64, "
+                            "128-slot pools, ring 16",
+                "verify_kernel_us": v["ver_ms"] * 1e3,
+                "verify_kernel_GBps": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9,
+                "verify_kernel_frac": v["ver_bytes"] / (v["ver_ms"] / 1e3) / 1e9 / hbm,
+                "fold_kernel_us": v["fold_ms"] * 1e3,
+            }
+        except Exception as e:  # noqa: BLE001
+            also["verify_fold_ragged"] = {"error": repr(e)}
         line["also"] = also
     if rank == 0:
         print(json.dumps(line), flush=True)

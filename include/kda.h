@@ -75,7 +75,8 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 } kda_dtype;
 enum {
     KDA_DEVERR_SLOT_RANGE = 1,   /* a slot id outside [0, num_slots) */
     KDA_DEVERR_ACCEPT_RANGE = 2, /* an accept length outside [0, max_accept] */
-    KDA_DEVERR_SEQLENS = 4,      /* cu_seqlens not monotone or past total_tokens */
+    KDA_DEVERR_SEQLENS = 4,      /* cu_seqlens or cu_drafts not monotone or past total_tokens,
+                                    or a draft count above G_max */
     KDA_DEVERR_RANGE = 8,        /* chunked prefill: a key channel's log-decay summed over half a
                                     chunk (32 tokens) is below -85, or a chunk intermediate
                                     (state, W, U) exceeds 60000 in magnitude: outside what the
@@ -225,6 +226,39 @@ KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, in
                                     int32_t *dev_err, void *stream);
 
 /*
+ * kda_verify_store_inputs_ragged -- verify with a draft count per request.
+ *
+ * Under load a per-step planner trims each request's verify window to the
+ * positions whose expected value covers their marginal cost, and the rest is
+ * cut before the target forward runs; what remains is verified exactly as
+ * before ("SGLang and Miles Add Day-0 Support for Kimi K3", section "Verify
+ * only what is worth verifying").  Request b verifies its own G_b tokens:
+ *
+ *   q, k, gk   device [total_tokens][H][K];  v, o device [total_tokens][H][V];
+ *              beta device [total_tokens][H]: request b's drafts are tokens
+ *              cu_drafts[b] .. cu_drafts[b+1]-1
+ *   cu_drafts  device int32 [B+1], non-decreasing, every G_b <= G_max and
+ *              cu_drafts[B] <= total_tokens; a request that breaks this is
+ *              skipped with KDA_DEVERR_SEQLENS
+ *   G_max      bound on every G_b (1 <= G_max <= ring->ring_len / 2); it picks
+ *              the kernel, so G_b = G_max for all b reproduces
+ *              kda_verify_store_inputs bit for bit
+ *   (other arguments as kda_verify_store_inputs)
+ * Record i < G_b goes to ring entry (ring_base[b] + i) mod ring_len; entries
+ * past G_b, and the o rows of no request, are not written.  G_b = 0 does
+ * nothing.  The committed state is never written.  kda_replay_fold is
+ * unchanged: it must be given accept_len[b] <= G_b.
+ */
+KDA_API int kda_verify_store_inputs_ragged(kda_dtype dt, int B, int G_max, int H, int K, int V,
+                                           const void *q, const void *k, const void *v,
+                                           const void *gk, const void *beta,
+                                           const int32_t *cu_drafts, int total_tokens,
+                                           const int32_t *slot_ids, const float *state_pool,
+                                           int num_slots, const kda_ring *ring,
+                                           const int32_t *ring_base, void *o, float scale,
+                                           int32_t *dev_err, void *stream);
+
+/*
  * kda_replay_fold -- commit the accepted prefix, all layers and heads, one launch.
  *
  * For every layer l, request b and head h: load the committed state from
@@ -245,6 +279,43 @@ KDA_API int kda_replay_fold(kda_dtype dt, int num_layers, int B, int H, int K, i
                             float *const *state_pools, const kda_ring *rings, int num_slots,
                             int max_accept, const int32_t *slot_ids, const int32_t *accept_len,
                             const int32_t *ring_base, int32_t *dev_err, void *stream);
+
+/*
+ * kda_verify_snapshot / kda_snapshot_commit -- the snapshot-per-step verify
+ * that ReplaySSM replaces, for comparing the two on the same workload.
+ *
+ * The baseline makes speculation reversible by saving the whole K x V state
+ * after every draft step, 64 KB per request, layer and head times the draft
+ * length, and the accepted length picks the saved state that becomes the slot
+ * ("SGLang and Miles Add Day-0 Support for Kimi K3", section "ReplaySSM:
+ * raw-input replay for the KDA state").
+ *
+ * kda_verify_snapshot: as kda_verify_store_inputs (same q, k, v, gk, beta, o,
+ * slot_ids, state_pool; the committed state is never written), but instead of
+ * ring records it writes the state after draft step i of request b to
+ *   snaps  device float [num_snap_slots][G][H][K][V] at [snap_ids[b]][i]
+ *   snap_ids device int32 [B], each in [0, num_snap_slots)
+ * with the per-token arithmetic of kda_decode_step: snapshot i is
+ * bit-identical to i + 1 decode steps.  1 <= G <= 64.
+ *
+ * kda_snapshot_commit: for every layer l and request b with a = accept_len[b]
+ * >= 1, copies snaps[l][snap_ids[b]][a - 1] (all H heads) over
+ * state_pools[l][slot_ids[b]]; a = 0 leaves the slot as it is.  One launch for
+ * all layers; state_pools and snaps are host arrays of num_layers device
+ * pointers (num_layers <= KDA_MAX_LAYERS).  accept_len outside [0, G] sets
+ * KDA_DEVERR_ACCEPT_RANGE and skips the request.
+ */
+KDA_API int kda_verify_snapshot(kda_dtype dt, int B, int G, int H, int K, int V, const void *q,
+                                const void *k, const void *v, const void *gk, const void *beta,
+                                const int32_t *slot_ids, const float *state_pool, int num_slots,
+                                float *snaps, const int32_t *snap_ids, int num_snap_slots,
+                                void *o, float scale, int32_t *dev_err, void *stream);
+
+KDA_API int kda_snapshot_commit(int num_layers, int B, int H, int K, int V, int G,
+                                float *const *state_pools, const float *const *snaps,
+                                int num_slots, int num_snap_slots, const int32_t *slot_ids,
+                                const int32_t *snap_ids, const int32_t *accept_len,
+                                int32_t *dev_err, void *stream);
 
 /*
  * kda_slot_copy -- dst slot <- src slot in every pool, bit-exact.

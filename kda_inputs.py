@@ -84,6 +84,12 @@ def accept_lengths(B: int, G: int, p: float, gen) -> torch.Tensor:
     return acc
 
 
+def draft_lengths(B: int, G: int, gen) -> torch.Tensor:
+    """Trimmed verify windows: a draft count per request, uniform on 1..G (the
+    pages give no distribution of the planner's window lengths)."""
+    return torch.randint(1, G + 1, (B,), generator=gen, device=gen.device).cpu().to(torch.int32)
+
+
 def slot_permutation(num_slots: int, gen) -> torch.Tensor:
     return torch.randperm(num_slots, generator=gen, device=gen.device).cpu().to(torch.int32)
 

@@ -24,8 +24,11 @@ from .binding import (  # noqa: F401
     kda_replay_fold,
     kda_ring,
     kda_slot_copy,
+    kda_snapshot_commit,
     kda_status_string,
     kda_verify_store_inputs,
+    kda_verify_store_inputs_ragged,
+    kda_verify_snapshot,
     lib,
     make_ring,
     record_bytes,

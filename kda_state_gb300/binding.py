@@ -63,11 +63,21 @@ def lib() -> ctypes.CDLL:
         L.kda_decode_step.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i, vp, f, ip, vp]
         L.kda_verify_store_inputs.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i,
                                               ctypes.POINTER(kda_ring), ip, vp, f, ip, vp]
+        L.kda_verify_store_inputs_ragged.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, i,
+                                                     ip, vp, i, ctypes.POINTER(kda_ring), ip, vp,
+                                                     f, ip, vp]
         L.kda_replay_fold.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_void_p),
                                       ctypes.POINTER(kda_ring), i, i, ip, ip, ip, ip, vp]
+        L.kda_verify_snapshot.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ip, vp, i, vp, ip,
+                                          i, vp, f, ip, vp]
+        L.kda_snapshot_commit.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_void_p),
+                                          ctypes.POINTER(ctypes.c_void_p), i, i, ip, ip, ip, ip,
+                                          vp]
         L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
                                     i, ip, vp]
         for fn in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step", "kda_verify_store_inputs",
+                   "kda_verify_store_inputs_ragged", "kda_verify_snapshot",
+                   "kda_snapshot_commit",
                    "kda_replay_fold", "kda_slot_copy"):
             getattr(L, fn).restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -233,6 +243,26 @@ def kda_verify_store_inputs(q, k, v, gk, beta, slot_ids, state_pool, ring: RingB
     return o
 
 
+def kda_verify_store_inputs_ragged(q, k, v, gk, beta, cu_drafts, G_max: int, slot_ids,
+                                   state_pool, ring: RingBuffers, ring_base=None, o=None,
+                                   scale: float = 1.0, dev_err=None, stream=None):
+    """Verify with G_b <= G_max drafts per request: q/k/gk [T, H, K], v [T, H, V],
+    beta [T, H] packed by cu_drafts (device int32 [B+1]).  Reads the pool, never
+    writes it; stores request b's G_b records into ``ring``.  Returns o [T, H, V]
+    (rows of no request are left as they were)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    B = cu_drafts.numel() - 1
+    if o is None:
+        o = torch.zeros(T, H, V, dtype=q.dtype, device=q.device)
+    desc = ring.descriptor()
+    _check("kda_verify_store_inputs_ragged", lib().kda_verify_store_inputs_ragged(
+        _dt(q), B, int(G_max), H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(cu_drafts), T,
+        _p(slot_ids), _p(state_pool), state_pool.shape[0], ctypes.byref(desc), _p(ring_base),
+        _p(o), float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
 def kda_replay_fold(state_pools, rings, slot_ids, accept_len, max_accept: int, ring_base=None,
                     dev_err=None, stream=None):
     """Fold the accepted prefixes of every layer in one launch.  state_pools: list
@@ -247,6 +277,42 @@ def kda_replay_fold(state_pools, rings, slot_ids, accept_len, max_accept: int, r
     _check("kda_replay_fold", lib().kda_replay_fold(
         _DT[rings[0].k.dtype], L, B, H, K, V, ptrs, descs, S, int(max_accept), _p(slot_ids),
         _p(accept_len), _p(ring_base), _p(dev_err), _stream(stream)))
+
+
+def kda_verify_snapshot(q, k, v, gk, beta, slot_ids, state_pool, snaps, snap_ids, o=None,
+                        scale: float = 1.0, dev_err=None, stream=None):
+    """Snapshot-per-step verify: q/k/gk [B, G, H, K], v [B, G, H, V], beta
+    [B, G, H]; writes the state after draft step i of request b to
+    snaps[snap_ids[b], i] (snaps fp32 [num_snap_slots, G, H, K, V]); never writes
+    the pool.  Returns o [B, G, H, V]."""
+    B, G, H, K = q.shape
+    V = v.shape[-1]
+    if snaps.shape[1] != G:
+        raise ValueError("snaps must be [num_snap_slots, G, H, K, V]")
+    if o is None:
+        o = torch.empty(B, G, H, V, dtype=q.dtype, device=q.device)
+    _check("kda_verify_snapshot", lib().kda_verify_snapshot(
+        _dt(q), B, G, H, K, V, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(slot_ids),
+        _p(state_pool), state_pool.shape[0], _p(snaps), _p(snap_ids), snaps.shape[0], _p(o),
+        float(scale), _p(dev_err), _stream(stream)))
+    return o
+
+
+def kda_snapshot_commit(state_pools, snaps, slot_ids, snap_ids, accept_len, dev_err=None,
+                        stream=None):
+    """Copy snapshot accept_len[b]-1 over slot slot_ids[b] in every layer, one
+    launch.  state_pools / snaps: lists of L pools [slots, H, K, V] and snapshot
+    buffers [num_snap_slots, G, H, K, V]."""
+    L = len(state_pools)
+    if L != len(snaps) or L == 0:
+        raise ValueError("state_pools and snaps must be non-empty lists of equal length")
+    S, H, K, V = state_pools[0].shape
+    NS, G = snaps[0].shape[0], snaps[0].shape[1]
+    pp = (ctypes.c_void_p * L)(*[p.data_ptr() for p in state_pools])
+    sp = (ctypes.c_void_p * L)(*[p.data_ptr() for p in snaps])
+    _check("kda_snapshot_commit", lib().kda_snapshot_commit(
+        L, slot_ids.numel(), H, K, V, G, pp, sp, S, NS, _p(slot_ids), _p(snap_ids),
+        _p(accept_len), _p(dev_err), _stream(stream)))
 
 
 def kda_slot_copy(pools, src, dst, dev_err=None, stream=None):

@@ -123,29 +123,57 @@ static bool ring_ok(const kda_ring *r, int G) {
     return G >= 1 && 2 * G <= R;
 }
 
-KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, int V,
-                                    const void *q, const void *k, const void *v, const void *gk,
-                                    const void *beta, const int32_t *slot_ids,
-                                    const float *state_pool, int num_slots, const kda_ring *ring,
-                                    const int32_t *ring_base, void *o, float scale,
-                                    int32_t *dev_err, void *stream) {
+static int verify_impl(kda_dtype dt, int B, int G, int H, int K, int V, const void *q,
+                       const void *k, const void *v, const void *gk, const void *beta,
+                       const int32_t *cu_drafts, int total_tokens, const int32_t *slot_ids,
+                       const float *state_pool, int num_slots, const kda_ring *ring,
+                       const int32_t *ring_base, void *o, float scale, int32_t *dev_err,
+                       void *stream) {
     if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
     if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
-    if (B < 0 || H < 1 || num_slots < 1 || G < 1 || G > 64 || !isfinite(scale))
+    if (B < 0 || H < 1 || num_slots < 1 || G < 1 || G > 64 || total_tokens < 0 ||
+        !isfinite(scale))
         return KDA_ERR_INVALID_ARG;
     if (!ring_ok(ring, G)) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
-    if (!q || !k || !v || !gk || !beta || !slot_ids || !state_pool || !o)
-        return KDA_ERR_INVALID_ARG;
+    if (!slot_ids || !state_pool) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !gk || !beta || !o)) return KDA_ERR_INVALID_ARG;
     if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
     if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     kda::VerifyArgs a;
     a.dt = dt; a.B = B; a.G = G; a.H = H; a.num_slots = num_slots; a.ring_len = ring->ring_len;
     a.q = q; a.k = k; a.v = v; a.gk = gk; a.beta = beta;
     a.slot_ids = slot_ids; a.ring_base = ring_base; a.pool = state_pool;
+    a.cu_drafts = cu_drafts; a.total_tokens = total_tokens;
     a.rk = ring->k; a.rv = ring->v; a.rdecay = ring->decay; a.rbeta = ring->beta;
     a.o = o; a.scale = scale; a.err = dev_err;
     return from_cuda(kda::launch_verify(a, (cudaStream_t)stream));
+}
+
+KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, int V,
+                                    const void *q, const void *k, const void *v, const void *gk,
+                                    const void *beta, const int32_t *slot_ids,
+                                    const float *state_pool, int num_slots, const kda_ring *ring,
+                                    const int32_t *ring_base, void *o, float scale,
+                                    int32_t *dev_err, void *stream) {
+    if (B > 0 && (!q || !k || !v || !gk || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * G > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    return verify_impl(dt, B, G, H, K, V, q, k, v, gk, beta, nullptr, B * G, slot_ids,
+                       state_pool, num_slots, ring, ring_base, o, scale, dev_err, stream);
+}
+
+KDA_API int kda_verify_store_inputs_ragged(kda_dtype dt, int B, int G_max, int H, int K, int V,
+                                           const void *q, const void *k, const void *v,
+                                           const void *gk, const void *beta,
+                                           const int32_t *cu_drafts, int total_tokens,
+                                           const int32_t *slot_ids, const float *state_pool,
+                                           int num_slots, const kda_ring *ring,
+                                           const int32_t *ring_base, void *o, float scale,
+                                           int32_t *dev_err, void *stream) {
+    if (B > 0 && !cu_drafts) return KDA_ERR_INVALID_ARG;
+    return verify_impl(dt, B, G_max, H, K, V, q, k, v, gk, beta, cu_drafts, total_tokens,
+                       slot_ids, state_pool, num_slots, ring, ring_base, o, scale, dev_err,
+                       stream);
 }
 
 KDA_API int kda_replay_fold(kda_dtype dt, int num_layers, int B, int H, int K, int V,
@@ -181,6 +209,57 @@ KDA_API int kda_replay_fold(kda_dtype dt, int num_layers, int B, int H, int K, i
         pp->layer[l].rbeta = rings[l].beta;
     }
     return from_cuda(kda::launch_fold(p, dt, (cudaStream_t)stream));
+}
+
+KDA_API int kda_verify_snapshot(kda_dtype dt, int B, int G, int H, int K, int V, const void *q,
+                                const void *k, const void *v, const void *gk, const void *beta,
+                                const int32_t *slot_ids, const float *state_pool, int num_slots,
+                                float *snaps, const int32_t *snap_ids, int num_snap_slots,
+                                void *o, float scale, int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || num_slots < 1 || num_snap_slots < 1 || G < 1 || G > 64 ||
+        !isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !gk || !beta || !slot_ids || !state_pool || !snaps || !snap_ids || !o)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool) || !aligned16(snaps)) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL || (long long)B * G > 0x7fffffffLL)
+        return KDA_ERR_INVALID_ARG;
+    kda::SnapVerifyArgs a;
+    a.dt = dt; a.B = B; a.G = G; a.H = H; a.num_slots = num_slots;
+    a.num_snap_slots = num_snap_slots;
+    a.q = q; a.k = k; a.v = v; a.gk = gk; a.beta = beta;
+    a.slot_ids = slot_ids; a.snap_ids = snap_ids; a.pool = state_pool; a.snaps = snaps;
+    a.o = o; a.scale = scale; a.err = dev_err;
+    return from_cuda(kda::launch_verify_snapshot(a, (cudaStream_t)stream));
+}
+
+KDA_API int kda_snapshot_commit(int num_layers, int B, int H, int K, int V, int G,
+                                float *const *state_pools, const float *const *snaps,
+                                int num_slots, int num_snap_slots, const int32_t *slot_ids,
+                                const int32_t *snap_ids, const int32_t *accept_len,
+                                int32_t *dev_err, void *stream) {
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (num_layers < 1 || num_layers > KDA_MAX_LAYERS || B < 0 || H < 1 || num_slots < 1 ||
+        num_snap_slots < 1 || G < 1 || G > 64)
+        return KDA_ERR_INVALID_ARG;
+    if (!state_pools || !snaps) return KDA_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l)
+        if (!state_pools[l] || !snaps[l] || !aligned16(state_pools[l]) || !aligned16(snaps[l]))
+            return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!slot_ids || !snap_ids || !accept_len) return KDA_ERR_INVALID_ARG;
+    kda::SnapCommitParams p;   // ~4 KB of pointers, copied into the launch parameters
+    p.L = num_layers; p.B = B; p.H = H; p.G = G; p.num_slots = num_slots;
+    p.num_snap_slots = num_snap_slots; p.chunks_per_copy = 0;
+    p.slot_ids = slot_ids; p.snap_ids = snap_ids; p.accept = accept_len; p.err = dev_err;
+    for (int l = 0; l < num_layers; ++l) {
+        p.pool[l] = state_pools[l];
+        p.snaps[l] = snaps[l];
+    }
+    return from_cuda(kda::launch_snapshot_commit(p, (cudaStream_t)stream));
 }
 
 KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems, int num_slots,

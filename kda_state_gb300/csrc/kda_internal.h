@@ -24,6 +24,10 @@ struct VerifyArgs {
     int dt, B, G, H, num_slots, ring_len;
     const void *q, *k, *v, *gk, *beta;
     const int32_t *slot_ids, *ring_base;
+    // ragged drafts: request b's tokens are cu_drafts[b] .. cu_drafts[b+1]-1 of
+    // [total_tokens][H][..] and number at most G; NULL: uniform [B][G][H][..]
+    const int32_t *cu_drafts;
+    int total_tokens;
     const float *pool;
     void *rk, *rv;
     float *rdecay, *rbeta;
@@ -69,7 +73,32 @@ struct PrefillArgs {
     const int32_t *ckpt_slots;     // device [N][max_ckpts]
 };
 
+// Snapshot-per-step verify: the state after every draft step into a
+// snapshot buffer [num_snap_slots][G][H][K][V].
+struct SnapVerifyArgs {
+    int dt, B, G, H, num_slots, num_snap_slots;
+    const void *q, *k, *v, *gk, *beta;
+    const int32_t *slot_ids, *snap_ids;
+    const float *pool;
+    float *snaps;
+    void *o;
+    float scale;
+    int32_t *err;
+};
+
+// Commit of the snapshot baseline: snapshot accept-1 -> the request's slot,
+// every layer, one launch.
+struct SnapCommitParams {
+    int L, B, H, G, num_slots, num_snap_slots, chunks_per_copy;
+    const int32_t *slot_ids, *snap_ids, *accept;
+    int32_t *err;
+    float *pool[KDA_MAX_LAYERS];
+    const float *snaps[KDA_MAX_LAYERS];
+};
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_verify_snapshot(const SnapVerifyArgs &a, cudaStream_t s);
+cudaError_t launch_snapshot_commit(const SnapCommitParams &p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s);
 cudaError_t launch_fold(const FoldParams &p, int dt, cudaStream_t s);
 cudaError_t launch_slot_copy(const CopyParams &p, cudaStream_t s);

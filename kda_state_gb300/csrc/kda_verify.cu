@@ -12,23 +12,40 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // verify: G draft tokens from the committed state, which is never written;
-// record i goes to ring entry (base + i) mod R of the request's slot.
+// record i goes to ring entry (base + i) mod R of the request's slot.  With
+// ragged drafts request b verifies its own G_b <= G tokens, packed by
+// cu_drafts; the uniform call is the case cu_drafts[b] = b G.
 // ---------------------------------------------------------------------------
+
+// Request b's first token and draft count; false (and an error bit) when the
+// ragged offsets are inconsistent.
+__device__ __forceinline__ bool draft_span(const VerifyArgs &a, int b, size_t &tok0, int &G) {
+    if (!a.cu_drafts) {
+        tok0 = (size_t)b * a.G;
+        G = a.G;
+        return true;
+    }
+    const int lo = a.cu_drafts[b], hi = a.cu_drafts[b + 1];
+    if (lo < 0 || hi < lo || hi - lo > a.G || hi > a.total_tokens) return false;
+    tok0 = (size_t)lo;
+    G = hi - lo;
+    return true;
+}
 
 // Recurrent form: the G tokens one after another on a register copy of the
 // state (the decode arithmetic).  Used for G > 16 and as the fallback of the
 // draft-block form below.
 template <typename T>
 __device__ __forceinline__ void verify_unit_recurrent(const VerifyArgs &a, int b, int h, int slot,
-                                                      unsigned char *smem) {
+                                                      size_t tok0, int G, unsigned char *smem) {
     Reduce &red = *reinterpret_cast<Reduce *>(smem);
     TokenIn *in = reinterpret_cast<TokenIn *>(smem + sizeof(Reduce));
     StateRegs r;
     state_load(r, a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS);
     const int base = a.ring_base ? a.ring_base[b] : 0;
     const int mask = a.ring_len - 1;
-    for (int i = 0; i < a.G; ++i) {
-        const size_t tok = ((size_t)b * a.G + i) * a.H + h;     // [B][G][H]
+    for (int i = 0; i < G; ++i) {
+        const size_t tok = (tok0 + i) * a.H + h;     // [tokens][H]
         const size_t e = ((size_t)slot * a.ring_len + ((base + i) & mask)) * a.H + h;
         stage_token<T, true>(in[i], (const T *)a.q + tok * KD, (const T *)a.k + tok * KD,
                              (const T *)a.v + tok * VD, (const T *)a.gk + tok * KD,
@@ -36,10 +53,10 @@ __device__ __forceinline__ void verify_unit_recurrent(const VerifyArgs &a, int b
                              a.rdecay + e * KD, a.rbeta + e);
     }
     __syncthreads();
-    for (int i = 0; i < a.G; ++i) {
+    for (int i = 0; i < G; ++i) {
         const float o = token_update<true>(r, in[i], red, a.scale);
         if (threadIdx.x < VD)
-            ((T *)a.o)[(((size_t)b * a.G + i) * a.H + h) * VD + threadIdx.x] = from_f<T>(o);
+            ((T *)a.o)[((tok0 + i) * a.H + h) * VD + threadIdx.x] = from_f<T>(o);
     }
 }
 
@@ -48,12 +65,19 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit - b * a.H;
+    size_t tok0;
+    int G;
+    if (!draft_span(a, b, tok0, G)) {
+        if (threadIdx.x == 0 && h == 0) report(a.err, DEVERR_SEQLENS);
+        return;
+    }
     const int slot = a.slot_ids[b];
     if (slot < 0 || slot >= a.num_slots) {
         if (threadIdx.x == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
         return;
     }
-    verify_unit_recurrent<T>(a, b, h, slot, smem);
+    if (G == 0) return;
+    verify_unit_recurrent<T>(a, b, h, slot, tok0, G, smem);
 }
 
 // Draft-block form (G <= GM): all G outputs from h0 at once.  With
@@ -88,13 +112,19 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
     VerifyBlockSmem<GM> &sm = *reinterpret_cast<VerifyBlockSmem<GM> *>(smem);
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit - b * a.H;
-    const int G = a.G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    size_t tok0;
+    int G;
+    if (!draft_span(a, b, tok0, G)) {
+        if (tid == 0 && h == 0) report(a.err, DEVERR_SEQLENS);
+        return;
+    }
     const int slot = a.slot_ids[b];
     if (slot < 0 || slot >= a.num_slots) {
         if (tid == 0 && h == 0) report(a.err, DEVERR_SLOT_RANGE);
         return;
     }
+    if (G == 0) return;
     // h0 into registers (read-only).  Tensor path (bf16 inputs, G <= 8): the B
     // fragments of m16n8k8 for this warp's 16 columns, as tf32.  CUDA-core path:
     // column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
@@ -128,7 +158,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
 #pragma unroll
         for (int i = 0; i < GM; ++i) {
             if (i < G) {
-                const size_t tok = ((size_t)b * G + i) * a.H + h;
+                const size_t tok = (tok0 + i) * a.H + h;
                 kr[i] = ((const T *)a.k)[tok * KD + c];
                 qr[i] = ((const T *)a.q)[tok * KD + c];
                 gr[i] = ((const T *)a.gk)[tok * KD + c];
@@ -158,7 +188,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
 #pragma unroll
         for (int i = 0; i < GM; ++i) {
             if (i < G) {
-                const size_t tok = ((size_t)b * G + i) * a.H + h;
+                const size_t tok = (tok0 + i) * a.H + h;
                 vr[i] = ((const T *)a.v)[tok * VD + c];
                 if (c == 0) br[i] = ((const T *)a.beta)[tok];
             }
@@ -182,7 +212,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         // The records above are the same ones the recurrent form stores; it
         // rewrites them identically.
         __syncthreads();
-        verify_unit_recurrent<T>(a, b, h, slot, smem);
+        verify_unit_recurrent<T>(a, b, h, slot, tok0, G, smem);
         return;
     }
     // Gram entries: pair p -> (r, j); pairs [0, G(G-1)/2) are A, the rest Aqk
@@ -277,7 +307,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                 }
             }
             if (g < G) {
-                T *dst = (T *)a.o + (((size_t)b * G + g) * a.H + h) * VD + c0;
+                T *dst = (T *)a.o + ((tok0 + g) * a.H + h) * VD + c0;
                 dst[0] = from_f<T>(a.scale * o0);
                 dst[1] = from_f<T>(a.scale * o1);
             }
@@ -318,7 +348,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
             float o = acc[GM + r];
 #pragma unroll
             for (int j = 0; j <= r; ++j) o = fmaf(sm.aqk[r][j], u[j], o);
-            ((T *)a.o)[(((size_t)b * G + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
+            ((T *)a.o)[((tok0 + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
         }
     }
 }

@@ -79,7 +79,8 @@ def load_variant(src_path: str, out_path: str):
     lib = _bind(build(force=True, src=src_path, out=out_path))
     import types
     ns = types.SimpleNamespace()
-    for name in ("unit", "prefill_varlen", "prefill_checkpoints", "decode", "verify", "fold"):
+    for name in ("unit", "prefill_varlen", "prefill_checkpoints", "decode", "verify",
+                 "verify_ragged", "fold"):
         fn = globals()[name]
         ns.__dict__[name] = (lambda f: (lambda *a, **kw: f(*a, _lib=lib, **kw)))(fn)
     return ns
@@ -247,6 +248,26 @@ def verify(q, k, v, gk, beta, S0, scale: float = 1.0, nthreads: int = 0, _lib=No
     o, _ = _batch(tok0, np.full(B * H, G), head, _seq_major(q), _seq_major(k), _seq_major(v),
                   _seq_major(gk), _seq_major(beta), S, scale, True, 0, nthreads, _lib)
     return o.reshape(v.shape)
+
+
+def verify_ragged(q, k, v, gk, beta, cu_drafts, S0, scale: float = 1.0, nthreads: int = 0,
+                  _lib=None):
+    """Verify with a draft count per request ("SGLang and Miles Add Day-0
+    Support for Kimi K3", section "Verify only what is worth verifying": the
+    planner trims each request's window, and what remains is verified exactly as
+    before).  q/k/gk [T, H, K], v [T, H, V], beta [T, H] packed by cu_drafts
+    [B+1]; S0 [B, H, K, V] (never modified).  Request b runs the recurrence over
+    its tokens cu_drafts[b] .. cu_drafts[b+1]-1 from S0[b].  Returns o [T, H, V]
+    (rows of no request stay zero)."""
+    q, k, v, gk, beta = (_f64(x) for x in (q, k, v, gk, beta))
+    cu = np.asarray(cu_drafts, dtype=np.int64)
+    B, H = len(cu) - 1, q.shape[1]
+    S = _f64(S0).reshape(B * H, *S0.shape[2:]).copy()   # scratch copy: S0 untouched
+    tok0 = np.repeat(cu[:-1], H)
+    head = np.tile(np.arange(H), B)
+    o, _ = _batch(tok0, np.repeat(cu[1:] - cu[:-1], H), head, q, k, v, gk, beta, S, scale, True,
+                  0, nthreads, _lib)
+    return o
 
 
 def fold(rec_k, rec_v, rec_gk, rec_beta, accept, S0, nthreads: int = 0, _lib=None):

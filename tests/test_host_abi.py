@@ -28,7 +28,8 @@ def declared_symbols():
 def test_header_declares_entry_points():
     names = declared_symbols()
     for n in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step",
-              "kda_verify_store_inputs", "kda_replay_fold", "kda_slot_copy", "kda_status_string"):
+              "kda_verify_store_inputs", "kda_verify_store_inputs_ragged", "kda_replay_fold",
+              "kda_verify_snapshot", "kda_snapshot_commit", "kda_slot_copy", "kda_status_string"):
         assert n in names
 
 
@@ -110,6 +111,14 @@ def test_verify_and_fold_ring_rules(L):
     ring.ring_len = 8                                              # 2 * G > R for G = 5
     assert L.kda_verify_store_inputs(0, 2, 5, 2, 128, 128, *(FAKE,) * 6, FAKE, 4, ctypes.byref(ring),
                                      None, FAKE, 1.0, None, None) == -1
+    ring.ring_len = 16
+    rag = lambda B, Gm, cu, T: (0, B, Gm, 2, 128, 128, *(FAKE,) * 5, cu, T, FAKE, FAKE, 4,
+                                ctypes.byref(ring), None, FAKE, 1.0, None, None)
+    assert L.kda_verify_store_inputs_ragged(*rag(2, 5, None, 6)) == -1    # no cu_drafts
+    assert L.kda_verify_store_inputs_ragged(*rag(2, 9, FAKE, 6)) == -1    # 2 * G_max > R
+    assert L.kda_verify_store_inputs_ragged(*rag(2, 0, FAKE, 6)) == -1    # G_max < 1
+    assert L.kda_verify_store_inputs_ragged(*rag(2, 5, FAKE, -1)) == -1   # negative tokens
+    assert L.kda_verify_store_inputs_ragged(*rag(0, 5, None, 0)) == 0     # empty batch
     rings = (kda.kda_ring * 2)(kda.kda_ring(4096, 4096, 4096, 4096, 16, 0),
                                kda.kda_ring(4096, 4096, 4096, 4096, 8, 0))   # ring lengths differ
     pools = (ctypes.c_void_p * 2)(4096, 4096)
@@ -122,6 +131,26 @@ def test_verify_and_fold_ring_rules(L):
                              None) == -1                             # no layers
     assert L.kda_replay_fold(0, 2, 0, 2, 128, 128, pools, rings, 4, 8, None, None, None, None,
                              None) == 0                              # empty batch
+
+
+def test_snapshot_baseline_rejects(L):
+    vs = lambda B, G, snaps, nsnap: (0, B, G, 2, 128, 128, *(FAKE,) * 5, FAKE, FAKE, 4, snaps, FAKE,
+                                     nsnap, FAKE, 1.0, None, None)
+    assert L.kda_verify_snapshot(*vs(2, 0, FAKE, 4)) == -1                   # G < 1
+    assert L.kda_verify_snapshot(*vs(2, 65, FAKE, 4)) == -1                  # G > 64
+    assert L.kda_verify_snapshot(*vs(2, 4, None, 4)) == -1                   # no snapshot buffer
+    assert L.kda_verify_snapshot(*vs(2, 4, ctypes.c_void_p(4100), 4)) == -1  # misaligned
+    assert L.kda_verify_snapshot(*vs(2, 4, FAKE, 0)) == -1                   # no snapshot slots
+    assert L.kda_verify_snapshot(*vs(0, 4, None, 4)) == 0                    # empty batch
+    pools = (ctypes.c_void_p * 2)(4096, 4096)
+    snaps = (ctypes.c_void_p * 2)(4096, None)
+    cm = lambda nl, B, G, sn: (nl, B, 2, 128, 128, G, pools, sn, 4, 4, FAKE, FAKE, FAKE, None, None)
+    assert L.kda_snapshot_commit(*cm(2, 2, 4, snaps)) == -1                  # a null snapshot buffer
+    snaps[1] = 4096
+    assert L.kda_snapshot_commit(*cm(0, 2, 4, snaps)) == -1                  # no layers
+    assert L.kda_snapshot_commit(*cm(257, 2, 4, snaps)) == -1                # too many layers
+    assert L.kda_snapshot_commit(*cm(2, 2, 0, snaps)) == -1                  # G < 1
+    assert L.kda_snapshot_commit(*cm(2, 0, 4, snaps)) == 0                   # empty batch
 
 
 def test_slot_copy_rejects(L):

@@ -259,6 +259,42 @@ def pin_checkpoints_are_prefix_states(orc):
     assert np.array_equal(o, o2) and np.array_equal(S, S2)
 
 
+def pin_ragged_verify_is_per_request_verify(orc):
+    """Ragged verify: request b's outputs are those of the recurrence over its
+    own G_b tokens from its committed state (brute-force matrix products of the
+    definition), rows of no request stay zero, the committed states are not
+    modified, and equal counts reproduce the uniform verify exactly."""
+    rng = _rng(14)
+    H, K, V, Gb = 2, 5, 4, [3, 0, 1, 4]
+    cu = np.concatenate([[1], 1 + np.cumsum(Gb)])      # token 0 belongs to no request
+    T = int(cu[-1]) + 4                                 # nor do the last four
+    q = rng.standard_normal((T, H, K))
+    k = rng.standard_normal((T, H, K))
+    v = rng.standard_normal((T, H, V))
+    gk = -rng.uniform(0, 1, (T, H, K))
+    beta = rng.uniform(0, 1, (T, H))
+    S0 = rng.standard_normal((len(Gb), H, K, V))
+    S0_copy = S0.copy()
+    o = orc.verify_ragged(q, k, v, gk, beta, cu, S0, scale=0.7)
+    assert np.array_equal(S0, S0_copy)
+    assert not o[0].any() and not o[-1].any()
+    for b in range(len(Gb)):
+        for h in range(H):
+            St = S0[b, h].copy()
+            for t in range(cu[b], cu[b + 1]):
+                P = np.eye(K) - beta[t, h] * np.outer(k[t, h], k[t, h])
+                St = P @ np.diag(np.exp(gk[t, h])) @ St + beta[t, h] * np.outer(k[t, h], v[t, h])
+                np.testing.assert_allclose(o[t, h], St.T @ (0.7 * q[t, h]), rtol=1e-12, atol=1e-13)
+    G = 3
+    assert len(Gb) * G <= T
+    cu_u = np.arange(len(Gb) + 1) * G
+    sl = slice(0, len(Gb) * G)
+    ou = orc.verify_ragged(q[sl], k[sl], v[sl], gk[sl], beta[sl], cu_u, S0, scale=0.7)
+    shp = lambda x: x[sl].reshape((len(Gb), G) + x.shape[1:])
+    ov = orc.verify(shp(q), shp(k), shp(v), shp(gk), shp(beta), S0, scale=0.7)
+    assert np.array_equal(ou, ov.reshape(ou.shape))
+
+
 PINS = [
     pin_single_token_closed_form,
     pin_identity_when_no_write_no_decay,
@@ -272,6 +308,7 @@ PINS = [
     pin_fold_is_prefix_commit,
     pin_batches_equal_units,
     pin_checkpoints_are_prefix_states,
+    pin_ragged_verify_is_per_request_verify,
 ]
 
 
