@@ -319,6 +319,126 @@ def bench_decode(args, ws, layers=69, B=384, H=64, slots=512, cow_frac=0.10, ste
                 layers=layers, n_cow=n_cow)
 
 
+def bench_decode_fused(args, ws, layers=69, B=384, H=64, slots=512, steps=None):
+    """Conv + KDA + onorm decode (one kda_decode_fused launch per layer) against
+    the unfused path (kda_conv_prologue + kda_decode_step + kda_gated_rmsnorm per
+    layer) on the same pools, conv states and raw inputs."""
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    g = gen.make_gen(3)
+    ids = gen.slot_permutation(slots, g)[:B].to(dev)
+    gd = gen.make_gen(1007, dev)
+    pools = [gen.checkpoint((slots, H, KD, VD), gd, device=dev) for _ in range(layers)]
+    convs = [gen.checkpoint((slots, 3, 3, H, KD), gd, device=dev, std=1.0).to(torch.bfloat16)
+             for _ in range(layers)]
+    xs = [{n: t[:, 0] for n, t in gen.raw_projections(1, H, torch.bfloat16, gd, device=dev,
+                                                        lead=(B,)).items()} for _ in range(layers)]
+    wts = [gen.fused_weights(H, torch.bfloat16, gd, device=dev) for _ in range(layers)]
+    out = torch.empty(B, H, VD, dtype=torch.bfloat16, device=dev)
+    q, k, v = (torch.empty(B, H, KD, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    beta = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    o = torch.empty(B, H, VD, dtype=torch.bfloat16, device=dev)
+    cu = torch.arange(B + 1, dtype=torch.int32)
+    cu_d = cu.to(dev)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(layers)]
+    record = {"on": False}
+    scale = KD ** -0.5
+
+    def step_fused():
+        for l in range(layers):
+            x, w = xs[l], wts[l]
+            if record["on"]:
+                ev[l][0].record(stream)
+            kda.kda_decode_fused(x["qkv"][:, 0], x["qkv"][:, 1], x["qkv"][:, 2], x["gk"], x["b"],
+                                 w["conv_w"], convs[l], x["gate"], w["w_norm"], ids, pools[l],
+                                 out=out, scale=scale)
+            if record["on"]:
+                ev[l][1].record(stream)
+
+    def step_unfused():
+        for l in range(layers):
+            x, w = xs[l], wts[l]
+            kda.kda_conv_prologue(x["qkv"][:, 0], x["qkv"][:, 1], x["qkv"][:, 2], x["b"],
+                                  w["conv_w"], convs[l], ids, ids, cu_d, cu, out=(q, k, v, beta))
+            kda.kda_decode_step(q, k, v, x["gk"], beta, ids, pools[l], o=o, scale=scale)
+            kda.kda_gated_rmsnorm(o, x["gate"], w["w_norm"], out=out)
+
+    K = steps or max(3, min(args.steps, 10))
+    ms_unfused = timed(step_unfused, K, 3, ws)
+    ms = timed(step_fused, K, 3, ws)
+    record["on"] = True
+    step_fused()
+    torch.cuda.synchronize()
+    record["on"] = False
+    fused_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    # per unit: state in + out, raw q k v, b, gk, gate, conv state in + out, normed o out
+    per_unit = 2 * STATE_B + 3 * KD * 2 + 2 + KD * 2 + VD * 2 + 2 * 3 * 3 * KD * 2 + VD * 2
+    del pools, convs, xs
+    torch.cuda.empty_cache()
+    return dict(ms=ms, ms_unfused=ms_unfused, fused_ms=fused_ms, fused_bytes=B * H * per_unit,
+                B=B, H=H, layers=layers)
+
+
+def bench_prefill_fused(args, ws):
+    """The varlen batch from raw projections: kda_conv_prologue, then
+    kda_chunk_prefill, then kda_gated_rmsnorm (the pages' prefill fusions around
+    FlashKDA), each timed on its own."""
+    import kda_state_gb300 as kda
+    dev = "cuda"
+    w = varlen_workload(dev)
+    N, H, T, cu_h = w["N"], w["H"], w["T"], w["cu"]
+    cu_d = cu_h.to(dev)
+    gd = gen.make_gen(1008, dev)
+    x = gen.raw_projections(T, H, torch.bfloat16, gd, device=dev)
+    wt = gen.fused_weights(H, torch.bfloat16, gd, device=dev)
+    conv = gen.checkpoint((2 * N, 3, 3, H, KD), gd, device=dev, std=1.0).to(torch.bfloat16)
+    pool = torch.empty(2 * N, H, KD, VD, device=dev)
+    pool[:N] = w["ck"]
+    init = torch.arange(N, dtype=torch.int32, device=dev)
+    out_s = torch.arange(N, 2 * N, dtype=torch.int32, device=dev)
+    q, k, v = (torch.empty(T, H, KD, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    beta = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    o = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    record = {"on": False}
+    scale = KD ** -0.5
+
+    def mark(i):
+        if record["on"]:
+            ev[i].record(stream)
+
+    def step():
+        mark(0)
+        kda.kda_conv_prologue(x["qkv"][:, 0], x["qkv"][:, 1], x["qkv"][:, 2], x["b"], wt["conv_w"],
+                              conv, init, out_s, cu_d, cu_h, out=(q, k, v, beta))
+        mark(1)
+        kda.kda_chunk_prefill(q, k, v, x["gk"], beta, cu_d, cu_h, pool, init, out_s, o=o,
+                              scale=scale)
+        mark(2)
+        kda.kda_gated_rmsnorm(o, x["gate"], wt["w_norm"], out=out)
+        mark(3)
+
+    K = max(3, min(args.steps, 200))
+    ms = timed(step, K, 3, ws)
+    times = []
+    for _ in range(5):
+        record["on"] = True
+        step()
+        torch.cuda.synchronize()
+        record["on"] = False
+        times.append([ev[i].elapsed_time(ev[i + 1]) for i in range(3)])
+    med = [statistics.median(t[i] for t in times) for i in range(3)]
+    th = T * H
+    pro_bytes = th * (3 * KD * 2 + 2 + 3 * KD * 2 + 2) + 2 * N * H * 3 * 3 * KD * 2
+    norm_bytes = th * 3 * VD * 2
+    return dict(ms=ms, T=T, prologue_ms=med[0], prefill_ms=med[1], norm_ms=med[2],
+                prologue_bytes=pro_bytes, norm_bytes=norm_bytes)
+
+
 def bench_verify_fold(args, ws, layers=69, B=64, G=8, H=64, slots=128, R=16, steps=None,
                       ragged=False):
     """Verify of B requests x G drafts on every layer, then one fold.  ragged:
@@ -564,8 +684,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the decode / verify+fold runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--only", choices=["decode", "verify", "verify_ragged", "snapshot_ab",
-                                       "checkpoints"],
+    ap.add_argument("--only", choices=["decode", "decode_fused", "prefill_fused", "verify",
+                                       "verify_ragged", "snapshot_ab", "checkpoints"],
                     default=None,
                     help="run one of the secondary workloads alone (for profiling)")
     ap.add_argument("--layers", type=int, default=69,
@@ -581,6 +701,10 @@ def main():
         _build.build()
         if args.only == "checkpoints":
             r = bench_varlen_checkpoints(args, 1)
+        elif args.only == "decode_fused":
+            r = bench_decode_fused(args, 1, layers=args.layers, steps=args.steps)
+        elif args.only == "prefill_fused":
+            r = bench_prefill_fused(args, 1)
         elif args.only == "snapshot_ab":
             r = bench_snapshot_ab(args, 1, layers=args.layers, steps=args.steps)
             r = {f"{a}_{k}": v for a, d in r.items() for k, v in d.items()}
@@ -709,6 +833,33 @@ def main():
             }
         except Exception as e:  # noqa: BLE001
             also["verify_fold"] = {"error": repr(e)}
+        try:
+            df = bench_decode_fused(args, ws)
+            also["decode_fused"] = {
+                "tok_per_s": df["B"] / (df["ms"] / 1e3) * ws, "ms_per_step": df["ms"],
+                "unfused_ms_per_step": df["ms_unfused"],
+                "workload": "384 req x 1 tok, H=64, 512-slot pools, 69 layers: conv + KDA + onorm "
+                            "in one launch per layer (unfused: prologue + decode + norm)",
+                "fused_kernel_us": df["fused_ms"] * 1e3,
+                "fused_kernel_GBps": df["fused_bytes"] / (df["fused_ms"] / 1e3) / 1e9,
+                "fused_kernel_frac": df["fused_bytes"] / (df["fused_ms"] / 1e3) / 1e9 / hbm,
+            }
+        except Exception as e:  # noqa: BLE001
+            also["decode_fused"] = {"error": repr(e)}
+        try:
+            pf = bench_prefill_fused(args, ws)
+            also["prefill_fused_path"] = {
+                "tok_per_s": pf["T"] / (pf["ms"] / 1e3) * ws, "ms_per_step": pf["ms"],
+                "workload": "the varlen batch from raw projections: conv prologue, chunked "
+                            "prefill, gated RMSNorm",
+                "prologue_us": pf["prologue_ms"] * 1e3,
+                "prologue_frac": pf["prologue_bytes"] / (pf["prologue_ms"] / 1e3) / 1e9 / hbm,
+                "prefill_us": pf["prefill_ms"] * 1e3,
+                "norm_us": pf["norm_ms"] * 1e3,
+                "norm_frac": pf["norm_bytes"] / (pf["norm_ms"] / 1e3) / 1e9 / hbm,
+            }
+        except Exception as e:  # noqa: BLE001
+            also["prefill_fused_path"] = {"error": repr(e)}
         try:
             ab = bench_snapshot_ab(args, ws)
             ab["workload"] = ("64 req x 8 draft tok, 69 layers, H=64, 128-slot pools: ReplaySSM "

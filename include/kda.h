@@ -318,6 +318,99 @@ KDA_API int kda_snapshot_commit(int num_layers, int B, int H, int K, int V, int 
                                 int32_t *dev_err, void *stream);
 
 /*
+ * Fused prologue and epilogue around the recurrence.
+ *
+ * Around each KDA layer the pages fuse small steps into single kernels, each
+ * bit-exact with the unfused path: the three short causal conv1d of q, k, v
+ * with SiLU and the conv-state update; the beta copy and sigmoid; the conv
+ * state gather and write-back; and the gated RMSNorm of the output read at its
+ * raw strides (Kimi K3 on B200 deployment notes, items "prefill / decode kernel
+ * fusion" and "other prefill switches"; "SGLang and Miles Add Day-0 Support for Kimi K3",
+ * ladder step P5 "Conv + KDA + Onorm Fusion" for decode).  The pages give
+ * neither the conv width nor the gate or norm formulas; this library uses:
+ *
+ *   conv     y_t[c] = sum_{i<W} w[c][i] x_{t-W+1+i}[c], W = KDA_CONV_WIDTH,
+ *            no bias; x before the sequence start comes from the conv state
+ *   SiLU     silu(y) = y / (1 + exp(-y))
+ *   q, k     L2-normalised per (token, head): x / sqrt(sum x^2 + eps_l2)
+ *   beta     sigmoid(b) = 1 / (1 + exp(-b))
+ *   o norm   out = w_norm[v] * o[v] / sqrt(mean_v o^2 + eps_norm) * sigmoid(g[v])
+ *
+ * Every intermediate that an unfused path would store (conv + SiLU output,
+ * normalised q and k, v, beta, o) is rounded to the dtype at the same point in
+ * the fused kernels, so kda_decode_fused equals kda_conv_prologue (one token
+ * per request) + kda_decode_step + kda_gated_rmsnorm bit for bit.
+ *
+ * Conv state pool: dtype [num_slots][KDA_CONV_WIDTH-1][3][H][K] -- for each
+ * slot, the last W-1 raw inputs of q, k and v (stream 0, 1, 2), oldest first.
+ * Conv weights: dtype [3][H][K][KDA_CONV_WIDTH].  (K = V = 128.)
+ *
+ * These kernels move 8 channels per 16-byte access: every device pointer must
+ * be 16-byte aligned and every stride a multiple of 16 bytes (else
+ * KDA_ERR_INVALID_ARG).
+ */
+#define KDA_CONV_WIDTH 4
+
+/*
+ * kda_conv_prologue -- conv + SiLU (+ L2 norm for q, k) and beta sigmoid for a
+ * packed varlen batch, with the conv state read from and written to slots.
+ *
+ *   q_raw, k_raw, v_raw device dtype: token t, head h, channel c at
+ *                   [t * raw_stride + h * K + c] (raw_stride >= H * K: the three
+ *                   may be views of one fused projection output)
+ *   b_raw           device dtype [total_tokens][H]
+ *   conv_w          device dtype [3][H][K][KDA_CONV_WIDTH]
+ *   conv_state      device dtype [num_slots][KDA_CONV_WIDTH-1][3][H][K]
+ *   init_slot       device int32 [N]: slot holding sequence n's conv state, or
+ *                   -1 for zeros
+ *   out_slot        device int32 [N]: slot receiving its state after the
+ *                   sequence, or -1 for none (may equal init_slot)
+ *   cu_seqlens_dev / _host  as kda_chunk_prefill
+ *   q, k, v         device dtype [total_tokens][H][K]; beta [total_tokens][H]
+ * Slots out of range skip the sequence with KDA_DEVERR_SLOT_RANGE.
+ */
+KDA_API int kda_conv_prologue(kda_dtype dt, int num_seqs, int total_tokens, int H, int K,
+                              const void *q_raw, const void *k_raw, const void *v_raw,
+                              long long raw_stride, const void *b_raw, const void *conv_w,
+                              void *conv_state, int num_slots, const int32_t *init_slot,
+                              const int32_t *out_slot, const int32_t *cu_seqlens_dev,
+                              const int32_t *cu_seqlens_host, void *q, void *k, void *v,
+                              void *beta, float eps_l2, int32_t *dev_err, void *stream);
+
+/*
+ * kda_gated_rmsnorm -- out = w_norm * o / sqrt(mean o^2 + eps) * sigmoid(g),
+ * per (token, head) row of V values.
+ *
+ *   o       device dtype, row (t, h) at [t * o_token_stride + h * o_head_stride]
+ *           (the attention output read at its own strides, no copy)
+ *   gate    device dtype [tokens][H][V];  w_norm device dtype [V]
+ *   out     device dtype [tokens][H][V]
+ */
+KDA_API int kda_gated_rmsnorm(kda_dtype dt, int tokens, int H, int V, const void *o,
+                              long long o_token_stride, long long o_head_stride,
+                              const void *gate, const void *w_norm, float eps, void *out,
+                              void *stream);
+
+/*
+ * kda_decode_fused -- conv + KDA + onorm: one token per request in one kernel.
+ *
+ * For request b (slot s = slot_ids[b]) and head h: conv of the new raw q, k, v
+ * with the slot's conv state (updated in place), SiLU, L2 norm of q and k, beta
+ * = sigmoid(b_raw), the decode step of kda_decode_step on the slot's KDA state
+ * (in place), and the gated RMSNorm of o into out.  raw inputs as
+ * kda_conv_prologue with one token per request; gk device dtype [B][H][K];
+ * gate [B][H][V]; out [B][H][V]; conv_state has num_slots slots like
+ * state_pool.  Bit-identical to the three unfused calls (see above).
+ */
+KDA_API int kda_decode_fused(kda_dtype dt, int B, int H, int K, int V, const void *q_raw,
+                             const void *k_raw, const void *v_raw, long long raw_stride,
+                             const void *gk, const void *b_raw, const void *conv_w,
+                             void *conv_state, const void *gate, const void *w_norm,
+                             const int32_t *slot_ids, float *state_pool, int num_slots,
+                             void *out, float scale, float eps_l2, float eps_norm,
+                             int32_t *dev_err, void *stream);
+
+/*
  * kda_slot_copy -- dst slot <- src slot in every pool, bit-exact.
  *
  * The copy-on-write restore and the snapshot of "Hybrid KDA Memory

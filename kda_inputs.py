@@ -14,6 +14,14 @@ Input recipe (all drawn in fp32 from one seeded ``torch.Generator``, then cast):
 * checkpoints ~ 0.02 * N(0, 1), fp32;
 * draw order: q, k, v, gk, beta (then checkpoints), so a seed fixes everything.
 
+Inputs of the fused prologue / epilogue (raw projection outputs and random-init
+weights; the pages give no trained values):
+
+* one fused q/k/v projection output [T, 3, H, K] ~ N(0, 1), read through views;
+* pre-sigmoid beta b ~ N(0, 1), output gate ~ N(0, 1), gk as above;
+* conv taps [3, H, K, 4] ~ 0.5 N(0, 1), RMSNorm weight ~ 1 + 0.1 N(0, 1);
+* conv states ~ N(0, 1) in the dtype.
+
 Workload shapes (K = V = 128):
 
 * tiny:    1 sequence, T = 64, H = 1, fp32, zero initial state, seed 0;
@@ -54,6 +62,32 @@ def token_inputs(T: int, H: int, dtype=torch.bfloat16, gen=None, device: str = "
     beta = torch.sigmoid(_normal(shp, gen, device))
     return {n: t.to(dtype).contiguous() for n, t in
             (("q", q), ("k", k), ("v", v), ("gk", gk), ("beta", beta))}
+
+
+def raw_projections(T: int, H: int, dtype=torch.bfloat16, gen=None, device: str = "cpu",
+                    K: int = K_DIM, lead=()):
+    """Inputs of the fused prologue / epilogue: one fused q/k/v projection
+    output qkv lead + [T, 3, H, K] ~ N(0, 1) (its [..., 0|1|2, :, :] slices are
+    the raw q, k, v), the pre-sigmoid beta b lead + [T, H] ~ N(0, 1), the output
+    gate lead + [T, H, K] ~ N(0, 1), and gk = -softplus(N(0, 1)) lead + [T, H, K]."""
+    gen = gen if gen is not None else make_gen(0, device)
+    shp = tuple(lead) + (T,)
+    qkv = _normal(shp + (3, H, K), gen, device)
+    b = _normal(shp + (H,), gen, device)
+    gate = _normal(shp + (H, K), gen, device)
+    gk = -torch.nn.functional.softplus(_normal(shp + (H, K), gen, device))
+    return {n: t.to(dtype).contiguous() for n, t in
+            (("qkv", qkv), ("b", b), ("gate", gate), ("gk", gk))}
+
+
+def fused_weights(H: int, dtype=torch.bfloat16, gen=None, device: str = "cpu", K: int = K_DIM,
+                  width: int = 4):
+    """Random-init weights of the prologue / epilogue: conv taps [3, H, K, width]
+    ~ 0.5 N(0, 1) and the RMSNorm weight [K] ~ 1 + 0.1 N(0, 1)."""
+    gen = gen if gen is not None else make_gen(0, device)
+    conv_w = 0.5 * _normal((3, H, K, width), gen, device)
+    w_norm = 1.0 + 0.1 * _normal((K,), gen, device)
+    return {"conv_w": conv_w.to(dtype).contiguous(), "w_norm": w_norm.to(dtype).contiguous()}
 
 
 def checkpoint(shape, gen, device: str = "cpu", std: float = 0.02) -> torch.Tensor:

@@ -20,7 +20,10 @@ from .binding import (  # noqa: F401
     RingBuffers,
     kda_chunk_prefill,
     kda_chunk_prefill_checkpoints,
+    kda_conv_prologue,
+    kda_decode_fused,
     kda_decode_step,
+    kda_gated_rmsnorm,
     kda_replay_fold,
     kda_ring,
     kda_slot_copy,
@@ -30,6 +33,7 @@ from .binding import (  # noqa: F401
     kda_verify_store_inputs_ragged,
     kda_verify_snapshot,
     lib,
+    make_conv_state,
     make_ring,
     record_bytes,
     ring_len_for,

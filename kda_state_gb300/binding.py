@@ -73,11 +73,18 @@ def lib() -> ctypes.CDLL:
         L.kda_snapshot_commit.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_void_p), i, i, ip, ip, ip, ip,
                                           vp]
+        ll = ctypes.c_longlong
+        L.kda_conv_prologue.argtypes = [i, i, i, i, i, vp, vp, vp, ll, vp, vp, vp, i, ip, ip, ip, ip,
+                                        vp, vp, vp, vp, f, ip, vp]
+        L.kda_gated_rmsnorm.argtypes = [i, i, i, i, vp, ll, ll, vp, vp, f, vp, vp]
+        L.kda_decode_fused.argtypes = [i, i, i, i, i, vp, vp, vp, ll, vp, vp, vp, vp, vp, vp, ip, vp,
+                                       i, vp, f, f, f, ip, vp]
         L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
                                     i, ip, vp]
         for fn in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step", "kda_verify_store_inputs",
                    "kda_verify_store_inputs_ragged", "kda_verify_snapshot",
-                   "kda_snapshot_commit",
+                   "kda_snapshot_commit", "kda_conv_prologue", "kda_gated_rmsnorm",
+                   "kda_decode_fused",
                    "kda_replay_fold", "kda_slot_copy"):
             getattr(L, fn).restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -313,6 +320,88 @@ def kda_snapshot_commit(state_pools, snaps, slot_ids, snap_ids, accept_len, dev_
     _check("kda_snapshot_commit", lib().kda_snapshot_commit(
         L, slot_ids.numel(), H, K, V, G, pp, sp, S, NS, _p(slot_ids), _p(snap_ids),
         _p(accept_len), _p(dev_err), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# fused prologue / epilogue around the recurrence
+# ---------------------------------------------------------------------------
+
+CONV_WIDTH = 4          # KDA_CONV_WIDTH
+EPS_L2 = 1e-6           # q, k L2 norm
+EPS_NORM = 1e-5         # gated RMSNorm of o
+
+
+def _raw_stride(q_raw, k_raw, v_raw, K):
+    """Token stride (elements) shared by three [T, H, K] raw views whose head
+    and channel axes are dense (e.g. slices of one fused projection output)."""
+    st = q_raw.stride(0)
+    for x in (q_raw, k_raw, v_raw):
+        if x.stride(-1) != 1 or x.stride(-2) != K or x.stride(0) != st:
+            raise ValueError("q_raw, k_raw, v_raw need dense [H, K] rows and one token stride")
+    return st
+
+
+def make_conv_state(num_slots: int, H: int, dtype=torch.bfloat16, device="cuda", K: int = K_DIM):
+    """Conv state pool [num_slots, W-1, 3, H, K] (zeros)."""
+    return torch.zeros(num_slots, CONV_WIDTH - 1, 3, H, K, dtype=dtype, device=device)
+
+
+def kda_conv_prologue(q_raw, k_raw, v_raw, b_raw, conv_w, conv_state, init_slot, out_slot,
+                      cu_seqlens, cu_seqlens_host, eps_l2: float = EPS_L2, out=None, dev_err=None,
+                      stream=None):
+    """Short conv + SiLU of q, k, v ([T, H, K] views sharing a token stride), L2
+    norm of q and k, beta = sigmoid(b_raw [T, H]); conv_w [3, H, K, W];
+    conv_state [slots, W-1, 3, H, K] read at init_slot and written at out_slot
+    (int32 [N] on the device, -1: zeros / none).  Returns (q, k, v, beta)."""
+    T, H, K = q_raw.shape
+    st = _raw_stride(q_raw, k_raw, v_raw, K)
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    N = host.numel() - 1
+    if out is None:
+        out = (torch.empty(T, H, K, dtype=q_raw.dtype, device=q_raw.device),
+               torch.empty(T, H, K, dtype=q_raw.dtype, device=q_raw.device),
+               torch.empty(T, H, K, dtype=q_raw.dtype, device=q_raw.device),
+               torch.empty(T, H, dtype=q_raw.dtype, device=q_raw.device))
+    q, k, v, beta = out
+    hp = host.numpy().ctypes.data_as(ctypes.c_void_p)
+    _check("kda_conv_prologue", lib().kda_conv_prologue(
+        _dt(q_raw), N, T, H, K, _p(q_raw), _p(k_raw), _p(v_raw), st, _p(b_raw), _p(conv_w),
+        _p(conv_state), conv_state.shape[0], _p(init_slot), _p(out_slot), _p(cu_seqlens), hp,
+        _p(q), _p(k), _p(v), _p(beta), float(eps_l2), _p(dev_err), _stream(stream)))
+    return q, k, v, beta
+
+
+def kda_gated_rmsnorm(o, gate, w_norm, eps: float = EPS_NORM, out=None, stream=None):
+    """out = w_norm * o / sqrt(mean o^2 + eps) * sigmoid(gate) per [token, head]
+    row; o [T, H, V] may be strided (channel axis dense)."""
+    T, H, V = o.shape
+    if o.stride(-1) != 1:
+        raise ValueError("o needs a dense channel axis")
+    if out is None:
+        out = torch.empty(T, H, V, dtype=o.dtype, device=o.device)
+    _check("kda_gated_rmsnorm", lib().kda_gated_rmsnorm(
+        _dt(o), T, H, V, _p(o), o.stride(0), o.stride(1), _p(gate), _p(w_norm), float(eps),
+        _p(out), _stream(stream)))
+    return out
+
+
+def kda_decode_fused(q_raw, k_raw, v_raw, gk, b_raw, conv_w, conv_state, gate, w_norm, slot_ids,
+                     state_pool, out=None, scale: float = 1.0, eps_l2: float = EPS_L2,
+                     eps_norm: float = EPS_NORM, dev_err=None, stream=None):
+    """Conv + KDA + onorm for one token per request: raw q, k, v [B, H, K]
+    (views sharing a token stride), gk, gate [B, H, K], b_raw [B, H]; the
+    slot's conv state and KDA state are updated in place.  Returns out [B, H, V]."""
+    B, H, K = q_raw.shape
+    V = state_pool.shape[-1]
+    st = _raw_stride(q_raw, k_raw, v_raw, K)
+    if out is None:
+        out = torch.empty(B, H, V, dtype=q_raw.dtype, device=q_raw.device)
+    _check("kda_decode_fused", lib().kda_decode_fused(
+        _dt(q_raw), B, H, K, V, _p(q_raw), _p(k_raw), _p(v_raw), st, _p(gk), _p(b_raw),
+        _p(conv_w), _p(conv_state), _p(gate), _p(w_norm), _p(slot_ids), _p(state_pool),
+        state_pool.shape[0], _p(out), float(scale), float(eps_l2), float(eps_norm), _p(dev_err),
+        _stream(stream)))
+    return out
 
 
 def kda_slot_copy(pools, src, dst, dev_err=None, stream=None):

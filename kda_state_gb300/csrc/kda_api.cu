@@ -1,6 +1,7 @@
 // C entry points of libkda.so: argument validation, launch parameters, and the
 // launch on the caller's stream.  No allocation, no synchronisation, no state.
 // The contract of every function is documented in include/kda.h.
+#include <algorithm>
 #include <math.h>
 #include <string.h>
 
@@ -260,6 +261,106 @@ KDA_API int kda_snapshot_commit(int num_layers, int B, int H, int K, int V, int 
         p.snaps[l] = snaps[l];
     }
     return from_cuda(kda::launch_snapshot_commit(p, (cudaStream_t)stream));
+}
+
+static bool cu_host_ok(const int32_t *cu, int N, int T) {
+    if (!cu || cu[0] != 0 || cu[N] != T) return false;
+    for (int n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return false;
+    return true;
+}
+
+KDA_API int kda_conv_prologue(kda_dtype dt, int num_seqs, int total_tokens, int H, int K,
+                              const void *q_raw, const void *k_raw, const void *v_raw,
+                              long long raw_stride, const void *b_raw, const void *conv_w,
+                              void *conv_state, int num_slots, const int32_t *init_slot,
+                              const int32_t *out_slot, const int32_t *cu_seqlens_dev,
+                              const int32_t *cu_seqlens_host, void *q, void *k, void *v,
+                              void *beta, float eps_l2, int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (K != 128) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H < 1 || num_slots < 1 || !(eps_l2 >= 0.f) ||
+        !isfinite(eps_l2))
+        return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (raw_stride < (long long)H * K) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens_dev || !cu_host_ok(cu_seqlens_host, num_seqs, total_tokens) || !conv_w ||
+        !conv_state || !init_slot || !out_slot)
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q_raw || !k_raw || !v_raw || !b_raw || !q || !k || !v || !beta))
+        return KDA_ERR_INVALID_ARG;
+    // 16-byte vectors of 8 channels: every row start must be 16-byte aligned
+    const long long vec = 16 / (dt == KDA_DTYPE_BF16 ? 2 : 4);
+    if (raw_stride % vec != 0 || !aligned16(conv_w) || !aligned16(conv_state)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(v_raw) ||
+                             !aligned16(q) || !aligned16(k) || !aligned16(v)))
+        return KDA_ERR_INVALID_ARG;
+    int max_len = 0;
+    for (int n = 0; n < num_seqs; ++n)
+        max_len = std::max(max_len, cu_seqlens_host[n + 1] - cu_seqlens_host[n]);
+    const int max_tiles = std::max(1, (max_len + 63) / 64);
+    if ((long long)num_seqs * max_tiles > 0x7fffffffLL || H > 65535) return KDA_ERR_INVALID_ARG;
+    kda::PrologueArgs a;
+    a.dt = dt; a.N = num_seqs; a.T_total = total_tokens; a.H = H; a.num_slots = num_slots;
+    a.max_tiles = max_tiles;
+    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.b_raw = b_raw; a.raw_stride = raw_stride;
+    a.conv_w = conv_w; a.conv_state = conv_state; a.init_slot = init_slot; a.out_slot = out_slot;
+    a.cu = cu_seqlens_dev; a.q = q; a.k = k; a.v = v; a.beta = beta; a.eps = eps_l2;
+    a.err = dev_err;
+    return from_cuda(kda::launch_conv_prologue(a, (cudaStream_t)stream));
+}
+
+KDA_API int kda_gated_rmsnorm(kda_dtype dt, int tokens, int H, int V, const void *o,
+                              long long o_token_stride, long long o_head_stride,
+                              const void *gate, const void *w_norm, float eps, void *out,
+                              void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (V != 128) return KDA_ERR_UNSUPPORTED;
+    if (tokens < 0 || H < 1 || !(eps >= 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARG;
+    if (tokens == 0) return KDA_OK;
+    if (!o || !gate || !w_norm || !out || o_token_stride < 0 || o_head_stride < 0)
+        return KDA_ERR_INVALID_ARG;
+    const long long vec = 16 / (dt == KDA_DTYPE_BF16 ? 2 : 4);
+    if (o_token_stride % vec != 0 || o_head_stride % vec != 0 || !aligned16(o) || !aligned16(gate) ||
+        !aligned16(w_norm) || !aligned16(out))
+        return KDA_ERR_INVALID_ARG;
+    kda::NormArgs a;
+    a.dt = dt; a.tokens = tokens; a.H = H; a.o = o; a.o_token_stride = o_token_stride;
+    a.o_head_stride = o_head_stride; a.gate = gate; a.w_norm = w_norm; a.eps = eps; a.out = out;
+    return from_cuda(kda::launch_gated_rmsnorm(a, (cudaStream_t)stream));
+}
+
+KDA_API int kda_decode_fused(kda_dtype dt, int B, int H, int K, int V, const void *q_raw,
+                             const void *k_raw, const void *v_raw, long long raw_stride,
+                             const void *gk, const void *b_raw, const void *conv_w,
+                             void *conv_state, const void *gate, const void *w_norm,
+                             const int32_t *slot_ids, float *state_pool, int num_slots,
+                             void *out, float scale, float eps_l2, float eps_norm,
+                             int32_t *dev_err, void *stream) {
+    if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || num_slots < 1 || !isfinite(scale) || !(eps_l2 >= 0.f) ||
+        !isfinite(eps_l2) || !(eps_norm >= 0.f) || !isfinite(eps_norm))
+        return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (raw_stride < (long long)H * K) return KDA_ERR_INVALID_ARG;
+    if (!q_raw || !k_raw || !v_raw || !gk || !b_raw || !conv_w || !conv_state || !gate ||
+        !w_norm || !slot_ids || !state_pool || !out)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    const long long vec = 16 / (dt == KDA_DTYPE_BF16 ? 2 : 4);
+    if (raw_stride % vec != 0 || !aligned16(q_raw) || !aligned16(k_raw) || !aligned16(v_raw) ||
+        !aligned16(gk) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(gate) ||
+        !aligned16(w_norm) || !aligned16(out))
+        return KDA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::FusedDecodeArgs a;
+    a.dt = dt; a.B = B; a.H = H; a.num_slots = num_slots;
+    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_stride = raw_stride;
+    a.gk = gk; a.b_raw = b_raw; a.conv_w = conv_w; a.conv_state = conv_state;
+    a.gate = gate; a.w_norm = w_norm; a.slot_ids = slot_ids; a.pool = state_pool; a.out = out;
+    a.scale = scale; a.eps_l2 = eps_l2; a.eps_norm = eps_norm; a.err = dev_err;
+    return from_cuda(kda::launch_decode_fused(a, (cudaStream_t)stream));
 }
 
 KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems, int num_slots,

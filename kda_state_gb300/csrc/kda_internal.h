@@ -96,6 +96,45 @@ struct SnapCommitParams {
     const float *snaps[KDA_MAX_LAYERS];
 };
 
+// Conv prologue over a packed varlen batch: grid (N x max_tiles, H).
+struct PrologueArgs {
+    int dt, N, T_total, H, num_slots, max_tiles;
+    const void *q_raw, *k_raw, *v_raw, *b_raw;
+    long long raw_stride;
+    const void *conv_w;
+    void *conv_state;
+    const int32_t *init_slot, *out_slot, *cu;
+    void *q, *k, *v, *beta;
+    float eps;
+    int32_t *err;
+};
+
+struct NormArgs {
+    int dt, tokens, H;
+    const void *o;
+    long long o_token_stride, o_head_stride;
+    const void *gate, *w_norm;
+    float eps;
+    void *out;
+};
+
+struct FusedDecodeArgs {
+    int dt, B, H, num_slots;
+    const void *q_raw, *k_raw, *v_raw;
+    long long raw_stride;
+    const void *gk, *b_raw, *conv_w;
+    void *conv_state;
+    const void *gate, *w_norm;
+    const int32_t *slot_ids;
+    float *pool;
+    void *out;
+    float scale, eps_l2, eps_norm;
+    int32_t *err;
+};
+
+cudaError_t launch_conv_prologue(const PrologueArgs &a, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(const NormArgs &a, cudaStream_t s);
+cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_verify_snapshot(const SnapVerifyArgs &a, cudaStream_t s);
 cudaError_t launch_snapshot_commit(const SnapCommitParams &p, cudaStream_t s);

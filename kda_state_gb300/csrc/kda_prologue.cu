@@ -1,0 +1,176 @@
+// Prologue and epilogue around the KDA recurrence for a packed batch: the short
+// causal conv of q, k, v with SiLU and the conv-state update, the L2 norm of q
+// and k, beta = sigmoid(b) (one kernel), and the gated RMSNorm of the output
+// read at its own strides (another).  Both move 16-byte vectors, 8 channels
+// per lane, and reduce each 128-channel row over a half-warp with the helpers
+// of kda_fused_ops.cuh.
+//
+// Paper correspondence: Kimi K3 on B200 deployment notes, items "prefill /
+// decode kernel fusion" and "other prefill switches": the three conv1d, the
+// beta copy + sigmoid and the conv-state gather / write-back fused into one
+// kernel, and the output layout copy folded into the gated RMSNorm, each
+// bit-exact with the unfused path.
+#include "kda_fused_ops.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int PRO_TILE = 64;                  // tokens per CTA
+constexpr int PRO_HEADS = 4;                  // heads per CTA
+constexpr int PRO_THREADS = 3 * 2 * 32;       // warp w: stream w / 2, heads 2 (w % 2) + lane / 16
+constexpr int PRO_PREFETCH = 8;               // tokens loaded ahead of the conv
+
+// grid: (N x max_tiles, ceil(H / 4)).  The CTA of tile 0 also reads the
+// sequence's conv state and writes the new one, so an in-place slot has one
+// reader and one writer, both in the same CTA.
+template <typename T>
+__global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const PrologueArgs a) {
+    const int tile = blockIdx.x % a.max_tiles, n = blockIdx.x / a.max_tiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = warp >> 1;
+    const int h = blockIdx.y * PRO_HEADS + 2 * (warp & 1) + (lane >> 4);
+    const int c0 = (lane & 15) * LANE_CH;
+    const bool live = h < a.H;   // a partial last head group leaves some half-warps idle
+    const int bos = a.cu[n], eos = a.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > a.T_total) {
+        if (threadIdx.x == 0 && tile == 0 && blockIdx.y == 0) report(a.err, DEVERR_SEQLENS);
+        return;
+    }
+    const int t0 = bos + tile * PRO_TILE;
+    if (tile > 0 && t0 >= eos) return;
+    const int si = a.init_slot[n], so = a.out_slot[n];
+    if (si < -1 || si >= a.num_slots || so < -1 || so >= a.num_slots) {
+        if (threadIdx.x == 0 && tile == 0 && blockIdx.y == 0) report(a.err, DEVERR_SLOT_RANGE);
+        return;
+    }
+    const int cnt = min(PRO_TILE, eos - t0);
+    const T *__restrict__ raw = (const T *)(s == 0 ? a.q_raw : s == 1 ? a.k_raw : a.v_raw);
+    T *__restrict__ dst = (T *)(s == 0 ? a.q : s == 1 ? a.k : a.v);
+    T *cs = (T *)a.conv_state;
+    const size_t col = (size_t)(live ? h : 0) * KD + c0;
+    const size_t hk = (size_t)a.H * KD;
+
+    Pack8<T> w[CONV_W], win[CONV_TAPS], init[CONV_TAPS];
+#pragma unroll
+    for (int i = 0; i < CONV_TAPS; ++i) zero8(init[i]);
+    if (live) {
+        load_taps((const T *)a.conv_w, s, a.H, h, c0, w);
+        if (tile == 0) {
+            if (si >= 0)
+#pragma unroll
+                for (int i = 0; i < CONV_TAPS; ++i) ld8(cs + conv_state_idx(si, i, s, a.H, h, c0), init[i]);
+#pragma unroll
+            for (int i = 0; i < CONV_TAPS; ++i) win[i] = init[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < CONV_TAPS; ++i)
+                ld8(raw + (size_t)(t0 - CONV_TAPS + i) * a.raw_stride + col, win[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < CONV_W; ++i) zero8(w[i]);
+#pragma unroll
+        for (int i = 0; i < CONV_TAPS; ++i) zero8(win[i]);
+    }
+    for (int j0 = 0; j0 < cnt; j0 += PRO_PREFETCH) {
+        Pack8<T> x[PRO_PREFETCH];
+#pragma unroll
+        for (int p = 0; p < PRO_PREFETCH; ++p) {
+            if (live && j0 + p < cnt)
+                ld8(raw + (size_t)(t0 + j0 + p) * a.raw_stride + col, x[p]);
+            else
+                zero8(x[p]);
+        }
+#pragma unroll
+        for (int p = 0; p < PRO_PREFETCH; ++p) {
+            if (j0 + p < cnt) {   // uniform across the CTA
+                float y[LANE_CH];
+                conv8<T>(w, win, x[p], y);
+                if (s < 2) l2norm8<T>(y, a.eps);
+                if (live) store8(dst + (size_t)(t0 + j0 + p) * hk + col, y);
+            }
+        }
+    }
+    if (s == 2 && live) {
+        for (int i = lane & 15; i < cnt; i += ROW_LANES) {
+            const size_t bi = (size_t)(t0 + i) * a.H + h;
+            ((T *)a.beta)[bi] = from_f<T>(sigmoid_f(to_f(((const T *)a.b_raw)[bi])));
+        }
+    }
+    if (tile == 0 && so >= 0 && live) {
+        // the last W-1 raw inputs of the sequence (from the old state where it is shorter)
+        const int len = eos - bos;
+#pragma unroll
+        for (int i = 0; i < CONV_TAPS; ++i) {
+            const int p = len - CONV_TAPS + i;   // position relative to the sequence start
+            Pack8<T> v = init[0];
+            if (p >= 0) {
+                ld8(raw + (size_t)(bos + p) * a.raw_stride + col, v);
+            } else {
+#pragma unroll
+                for (int m = 1; m < CONV_TAPS; ++m)
+                    if (m == p + CONV_TAPS) v = init[m];
+            }
+            st8(cs + conv_state_idx(so, i, s, a.H, h, c0), v);
+        }
+    }
+}
+
+// Grid-stride over pairs of (token, head) rows: one row per half-warp.
+template <typename T>
+__global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormArgs a) {
+    const int lane = threadIdx.x & 31, c0 = (lane & 15) * LANE_CH;
+    const size_t rows = (size_t)a.tokens * a.H;
+    float wn[LANE_CH];
+    load8((const T *)a.w_norm + c0, wn);
+    const size_t nwarps = (size_t)gridDim.x * (CTA_THREADS / 32);
+    for (size_t pair = (size_t)blockIdx.x * (CTA_THREADS / 32) + (threadIdx.x >> 5); pair * 2 < rows;
+         pair += nwarps) {
+        const size_t row = pair * 2 + (lane >> 4);
+        const bool live = row < rows;
+        float o[LANE_CH], g[LANE_CH];
+        if (live) {
+            const size_t t = row / a.H, h = row - t * a.H;
+            load8((const T *)a.o + t * a.o_token_stride + h * a.o_head_stride + c0, o);
+            load8((const T *)a.gate + row * VD + c0, g);
+        } else {
+#pragma unroll
+            for (int e = 0; e < LANE_CH; ++e) o[e] = g[e] = 0.f;
+        }
+        const float f = rms_factor(row_sumsq(o), a.eps);
+        float y[LANE_CH];
+#pragma unroll
+        for (int e = 0; e < LANE_CH; ++e) y[e] = gated_norm(o[e], f, wn[e], g[e]);
+        if (live) store8((T *)a.out + row * VD + c0, y);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_conv_prologue(const PrologueArgs &a, cudaStream_t s) {
+    const dim3 grid((unsigned)(a.N * a.max_tiles), (unsigned)((a.H + PRO_HEADS - 1) / PRO_HEADS));
+    if (a.dt == KDA_DTYPE_BF16)
+        conv_prologue_kernel<__nv_bfloat16><<<grid, PRO_THREADS, 0, s>>>(a);
+    else
+        conv_prologue_kernel<float><<<grid, PRO_THREADS, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gated_rmsnorm(const NormArgs &a, cudaStream_t s) {
+    const size_t rows = (size_t)a.tokens * a.H;
+    if (rows == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t want = (rows + 15) / 16;   // warps of 2 rows, 8 warps per CTA
+    const size_t cap = (size_t)(sms > 0 ? sms : 152) * 8;
+    const unsigned grid = (unsigned)(want < cap ? want : cap);
+    if (a.dt == KDA_DTYPE_BF16)
+        gated_rmsnorm_kernel<__nv_bfloat16><<<grid, CTA_THREADS, 0, s>>>(a);
+    else
+        gated_rmsnorm_kernel<float><<<grid, CTA_THREADS, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

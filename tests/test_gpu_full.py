@@ -111,6 +111,45 @@ def test_varlen_prefill_checkpoints_full():
                          "checkpoint %d of sequence %d" % (m, n))
 
 
+def test_decode_fused_full_layer():
+    """One layer of the decode workload (384 requests x 64 heads, 512-slot
+    pools) through conv + KDA + onorm, launched as the benchmark launches it:
+    bit-identical to prologue + decode step + norm; untouched slots unchanged;
+    the outputs of 16 requests vs the oracle (bf16 intermediates stored as the
+    unfused path stores them)."""
+    from oracle import fused_ops as fo
+    B, H, S = 384, 64, 512
+    g = gen.make_gen(3)
+    ids = gen.slot_permutation(S, g)[:B].to(DEV)
+    gd = gen.make_gen(1007, DEV)
+    pool0 = gen.checkpoint((S, H, KD, VD), gd, device=DEV)
+    cs0 = gen.checkpoint((S, 3, 3, H, KD), gd, device=DEV, std=1.0).to(torch.bfloat16)
+    x = {n: t[:, 0] for n, t in gen.raw_projections(1, H, torch.bfloat16, gd, device=DEV,
+                                                      lead=(B,)).items()}
+    w = gen.fused_weights(H, torch.bfloat16, gd, device=DEV)
+    raw = (x["qkv"][:, 0], x["qkv"][:, 1], x["qkv"][:, 2])
+    scale = KD ** -0.5
+    pool_f, cs_f = pool0.clone(), cs0.clone()
+    out_f = kda().kda_decode_fused(*raw, x["gk"], x["b"], w["conv_w"], cs_f, x["gate"], w["w_norm"],
+                                   ids, pool_f, scale=scale)
+    pool_u, cs_u = pool0.clone(), cs0.clone()
+    cu = torch.arange(B + 1, dtype=torch.int32)
+    q, k, v, beta = kda().kda_conv_prologue(*raw, x["b"], w["conv_w"], cs_u, ids, ids, cu.to(DEV), cu)
+    o = kda().kda_decode_step(q, k, v, x["gk"], beta, ids, pool_u, scale=scale)
+    out_u = kda().kda_gated_rmsnorm(o, x["gate"], w["w_norm"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_f, out_u) and torch.equal(pool_f, pool_u) and torch.equal(cs_f, cs_u)
+    other = torch.ones(S, dtype=torch.bool, device=DEV)
+    other[ids.long()] = False
+    assert torch.equal(pool_f[other], pool0[other]) and torch.equal(cs_f[other], cs0[other])
+    sel = torch.arange(0, B, B // 16, device=DEV)[:16]
+    sid = ids[sel].long()
+    ref_out, _, _ = fo.decode_fused(*(f64(t[sel]) for t in raw), f64(x["gk"][sel]), f64(x["b"][sel]),
+                                    f64(w["conv_w"]), f64(cs0), f64(x["gate"][sel]), f64(w["w_norm"]),
+                                    sid.cpu().numpy(), f64(pool0), scale=scale, store=fo.round_bf16)
+    assert_close(out_f[sel], ref_out, torch.bfloat16, "fused decode out")
+
+
 def test_long_prefill_pieces_full():
     """4 sequences x 24576 tokens, H = 96, bf16, from checkpoints, as six
     pieces of 4096 tokens that resume in place; after each piece the state is

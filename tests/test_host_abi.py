@@ -29,7 +29,8 @@ def test_header_declares_entry_points():
     names = declared_symbols()
     for n in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step",
               "kda_verify_store_inputs", "kda_verify_store_inputs_ragged", "kda_replay_fold",
-              "kda_verify_snapshot", "kda_snapshot_commit", "kda_slot_copy", "kda_status_string"):
+              "kda_verify_snapshot", "kda_snapshot_commit", "kda_conv_prologue",
+              "kda_gated_rmsnorm", "kda_decode_fused", "kda_slot_copy", "kda_status_string"):
         assert n in names
 
 
@@ -151,6 +152,31 @@ def test_snapshot_baseline_rejects(L):
     assert L.kda_snapshot_commit(*cm(257, 2, 4, snaps)) == -1                # too many layers
     assert L.kda_snapshot_commit(*cm(2, 2, 0, snaps)) == -1                  # G < 1
     assert L.kda_snapshot_commit(*cm(2, 0, 4, snaps)) == 0                   # empty batch
+
+
+def test_fused_prologue_epilogue_rejects(L):
+    cu = _cu([0, 5, 9])
+    pro = lambda dt, K, stride, cuh, eps: (dt, 2, 9, 2, K, FAKE, FAKE, FAKE, stride, FAKE, FAKE,
+                                           FAKE, 4, FAKE, FAKE, FAKE, cuh, FAKE, FAKE, FAKE, FAKE,
+                                           eps, None, None)
+    assert L.kda_conv_prologue(*pro(3, 128, 256, cu, 1e-6)) == -2        # bad dtype
+    assert L.kda_conv_prologue(*pro(0, 64, 256, cu, 1e-6)) == -2         # K != 128
+    assert L.kda_conv_prologue(*pro(0, 128, 255, cu, 1e-6)) == -1        # stride < H * K
+    assert L.kda_conv_prologue(*pro(0, 128, 256, _cu([0, 5, 3]), 1e-6)) == -1
+    assert L.kda_conv_prologue(*pro(0, 128, 256, None, 1e-6)) == -1      # host copy required
+    assert L.kda_conv_prologue(*pro(0, 128, 256, cu, -1.0)) == -1        # negative eps
+    assert L.kda_conv_prologue(*pro(0, 128, 256, cu, float("nan"))) == -1
+    nrm = lambda V, T, o, eps: (0, T, 2, V, o, 256, 128, FAKE, FAKE, eps, FAKE, None)
+    assert L.kda_gated_rmsnorm(*nrm(64, 3, FAKE, 1e-5)) == -2            # V != 128
+    assert L.kda_gated_rmsnorm(*nrm(128, 3, None, 1e-5)) == -1           # no o
+    assert L.kda_gated_rmsnorm(*nrm(128, 3, FAKE, -1e-5)) == -1
+    assert L.kda_gated_rmsnorm(*nrm(128, 0, None, 1e-5)) == 0            # nothing to do
+    dec = lambda B, stride, pool: (0, B, 2, 128, 128, FAKE, FAKE, FAKE, stride, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, FAKE, FAKE, pool, 4, FAKE, 1.0, 1e-6, 1e-5, None,
+                                   None)
+    assert L.kda_decode_fused(*dec(2, 255, FAKE)) == -1                  # stride < H * K
+    assert L.kda_decode_fused(*dec(2, 256, ctypes.c_void_p(4100))) == -1 # misaligned pool
+    assert L.kda_decode_fused(*dec(0, 256, None)) == 0                   # empty batch
 
 
 def test_slot_copy_rejects(L):
