@@ -318,6 +318,7 @@ KDA_API int kda_gated_rmsnorm(kda_dtype dt, int tokens, int H, int V, const void
     if (V != 128) return KDA_ERR_UNSUPPORTED;
     if (tokens < 0 || H < 1 || !(eps >= 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARG;
     if (tokens == 0) return KDA_OK;
+    if ((long long)tokens * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (!o || !gate || !w_norm || !out || o_token_stride < 0 || o_head_stride < 0)
         return KDA_ERR_INVALID_ARG;
     const long long vec = 16 / (dt == KDA_DTYPE_BF16 ? 2 : 4);

@@ -21,16 +21,25 @@ constexpr int CONV_TAPS = CONV_W - 1;   // raw inputs kept in the conv state
 constexpr int ROW_LANES = 16;           // lanes per 128-channel row
 constexpr int LANE_CH = 8;              // channels per lane
 
-// The fast exponential and division intrinsics (a few instructions each, about
-// 2 ulp); every kernel calls these same two helpers, so the fused and unfused
-// paths stay bit-identical.  A denominator beyond 2^126 (exp(-x) overflowing)
-// gives 0, the limit of both functions there.
+// exp(-x) as 2^(-x log2 e) (a change of base) on the PTX ex2.approx
+// instruction, and 1 / d on rcp.approx: a few instructions, relative error
+// near 2^-22.  Every kernel calls these same helpers, so the fused and
+// unfused paths stay bit-identical.  For a large negative argument exp(-x)
+// overflows to +inf and the reciprocal gives 0, the limit of both functions.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float sigmoid_f(float x) {
-    return __fdividef(1.f, __fadd_rn(1.f, __expf(-x)));
+    return rcp_approx(__fadd_rn(1.f, ex2_approx(__fmul_rn(x, -1.4426950408889634f))));
 }
-__device__ __forceinline__ float silu_f(float y) {
-    return __fdividef(y, __fadd_rn(1.f, __expf(-y)));
-}
+__device__ __forceinline__ float silu_f(float y) { return __fmul_rn(y, sigmoid_f(y)); }
 
 // The value an unfused path would store and read back.
 template <typename T>
@@ -129,9 +138,11 @@ __device__ __forceinline__ float row_sumsq(const float (&x)[LANE_CH]) {
 // 1 / sqrt(sum of squares + eps): the L2-norm factor of q and k.
 __device__ __forceinline__ float l2_factor(float ss, float eps) { return rsqrtf(__fadd_rn(ss, eps)); }
 
-// 1 / sqrt(mean of squares + eps) over V channels: the RMSNorm factor.
+// 1 / sqrt(mean of squares + eps) over V channels: the RMSNorm factor (the
+// mean is an exact scaling by 2^-7).
 __device__ __forceinline__ float rms_factor(float ss, float eps) {
-    return rsqrtf(__fadd_rn(__fdiv_rn(ss, (float)VD), eps));
+    static_assert(VD == 128, "the mean scales by 2^-7");
+    return rsqrtf(__fadd_rn(__fmul_rn(ss, 0.0078125f), eps));
 }
 
 // One channel of the gated RMSNorm output.
@@ -146,7 +157,8 @@ __device__ __forceinline__ size_t conv_state_idx(int slot, int tap, int stream, 
 
 // The W taps of 8 channels c0 .. c0+7 of one stream and head: 8 x W elements,
 // contiguous in conv_w [3][H][K][W] (16-byte aligned); tap i of channel e is
-// element (e W + i) of the run.
+// element (e W + i) of the run.  Kept packed (load_taps) or unpacked once into
+// floats (unpack_taps) -- the values are the same.
 template <typename T>
 __device__ __forceinline__ void load_taps(const T *conv_w, int stream, int H, int h, int c0,
                                           Pack8<T> (&w)[CONV_W]) {
@@ -154,24 +166,54 @@ __device__ __forceinline__ void load_taps(const T *conv_w, int stream, int H, in
 #pragma unroll
     for (int i = 0; i < CONV_W; ++i) ld8(p + i * LANE_CH, w[i]);
 }
+template <typename T>
+__device__ __forceinline__ void unpack_taps(const Pack8<T> (&p)[CONV_W], float (&w)[LANE_CH][CONV_W]) {
+#pragma unroll
+    for (int e = 0; e < LANE_CH; ++e)
+#pragma unroll
+        for (int i = 0; i < CONV_W; ++i) w[e][i] = el(p[(e * CONV_W + i) / LANE_CH], (e * CONV_W + i) % LANE_CH);
+}
+template <typename T>
+__device__ __forceinline__ float tap(const Pack8<T> (&w)[CONV_W], int e, int i) {
+    return el(w[(e * CONV_W + i) / LANE_CH], (e * CONV_W + i) % LANE_CH);
+}
+__device__ __forceinline__ float tap(const float (&w)[LANE_CH][CONV_W], int e, int i) { return w[e][i]; }
+
+// Conv windows (the W-1 previous raw inputs of 8 channels): packed rows or
+// floats, with the same values.
+template <typename T>
+__device__ __forceinline__ float wget(const Pack8<T> (&win)[CONV_TAPS], int i, int e) { return el(win[i], e); }
+__device__ __forceinline__ float wget(const float (&win)[CONV_TAPS][LANE_CH], int i, int e) { return win[i][e]; }
+template <typename T>
+__device__ __forceinline__ void wshift(Pack8<T> (&win)[CONV_TAPS], const Pack8<T> &x) {
+#pragma unroll
+    for (int i = 0; i + 1 < CONV_TAPS; ++i) win[i] = win[i + 1];
+    win[CONV_TAPS - 1] = x;
+}
+template <typename T>
+__device__ __forceinline__ void wshift(float (&win)[CONV_TAPS][LANE_CH], const Pack8<T> &x) {
+#pragma unroll
+    for (int e = 0; e < LANE_CH; ++e) {
+#pragma unroll
+        for (int i = 0; i + 1 < CONV_TAPS; ++i) win[i][e] = win[i + 1][e];
+        win[CONV_TAPS - 1][e] = el(x, e);
+    }
+}
 
 // Conv + SiLU of one token on 8 channels; shifts x into the window.  y gets
 // the outputs rounded to T (the stored conv output).
-template <typename T>
-__device__ __forceinline__ void conv8(const Pack8<T> (&w)[CONV_W], Pack8<T> (&win)[CONV_TAPS],
-                                      const Pack8<T> &x, float (&y)[LANE_CH]) {
+template <typename T, typename Taps, typename Win>
+__device__ __forceinline__ void conv8(const Taps &w, Win &win, const Pack8<T> &x, float (&y)[LANE_CH]) {
 #pragma unroll
     for (int e = 0; e < LANE_CH; ++e) {
         float wt[CONV_W], wv[CONV_TAPS];
 #pragma unroll
-        for (int i = 0; i < CONV_W; ++i) wt[i] = el(w[(e * CONV_W + i) / LANE_CH], (e * CONV_W + i) % LANE_CH);
+        for (int i = 0; i < CONV_W; ++i) wt[i] = tap(w, e, i);
 #pragma unroll
-        for (int i = 0; i < CONV_TAPS; ++i) wv[i] = el(win[i], e);
+        for (int i = 0; i < CONV_TAPS; ++i) wv[i] = wget(win, i, e);
         y[e] = round_t<T>(conv_silu(wt, wv, el(x, e)));
     }
-#pragma unroll
-    for (int i = 0; i + 1 < CONV_TAPS; ++i) win[i] = win[i + 1];
-    win[CONV_TAPS - 1] = x;
+    wshift(win, x);
 }
 
 // L2-normalise a rounded q or k row (every lane of the warp must call it).

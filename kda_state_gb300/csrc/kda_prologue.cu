@@ -17,19 +17,19 @@ namespace kda {
 namespace {
 
 constexpr int PRO_TILE = 64;                  // tokens per CTA
-constexpr int PRO_HEADS = 4;                  // heads per CTA
-constexpr int PRO_THREADS = 3 * 2 * 32;       // warp w: stream w / 2, heads 2 (w % 2) + lane / 16
-constexpr int PRO_PREFETCH = 8;               // tokens loaded ahead of the conv
+constexpr int PRO_HEADS = 2;                  // heads per CTA
+constexpr int PRO_THREADS = 3 * 32;           // warp w: stream w, heads lane / 16
+constexpr int PRO_PREFETCH = 4;               // tokens loaded ahead of the conv
 
-// grid: (N x max_tiles, ceil(H / 4)).  The CTA of tile 0 also reads the
+// grid: (N x max_tiles, ceil(H / 2)).  The CTA of tile 0 also reads the
 // sequence's conv state and writes the new one, so an in-place slot has one
 // reader and one writer, both in the same CTA.
 template <typename T>
 __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const PrologueArgs a) {
     const int tile = blockIdx.x % a.max_tiles, n = blockIdx.x / a.max_tiles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = warp >> 1;
-    const int h = blockIdx.y * PRO_HEADS + 2 * (warp & 1) + (lane >> 4);
+    const int s = warp;
+    const int h = blockIdx.y * PRO_HEADS + (lane >> 4);
     const int c0 = (lane & 15) * LANE_CH;
     const bool live = h < a.H;   // a partial last head group leaves some half-warps idle
     const int bos = a.cu[n], eos = a.cu[n + 1];
@@ -51,27 +51,31 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
     const size_t col = (size_t)(live ? h : 0) * KD + c0;
     const size_t hk = (size_t)a.H * KD;
 
-    Pack8<T> w[CONV_W], win[CONV_TAPS], init[CONV_TAPS];
+    // taps and windows unpacked once: every token reuses them
+    float w[LANE_CH][CONV_W], win[CONV_TAPS][LANE_CH];
+    {
+        Pack8<T> wp[CONV_W], wn[CONV_TAPS];
 #pragma unroll
-    for (int i = 0; i < CONV_TAPS; ++i) zero8(init[i]);
-    if (live) {
-        load_taps((const T *)a.conv_w, s, a.H, h, c0, w);
-        if (tile == 0) {
-            if (si >= 0)
+        for (int i = 0; i < CONV_W; ++i) zero8(wp[i]);
 #pragma unroll
-                for (int i = 0; i < CONV_TAPS; ++i) ld8(cs + conv_state_idx(si, i, s, a.H, h, c0), init[i]);
+        for (int i = 0; i < CONV_TAPS; ++i) zero8(wn[i]);
+        if (live) {
+            load_taps((const T *)a.conv_w, s, a.H, h, c0, wp);
+            if (tile == 0) {
+                if (si >= 0)
 #pragma unroll
-            for (int i = 0; i < CONV_TAPS; ++i) win[i] = init[i];
-        } else {
+                    for (int i = 0; i < CONV_TAPS; ++i) ld8(cs + conv_state_idx(si, i, s, a.H, h, c0), wn[i]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < CONV_TAPS; ++i)
-                ld8(raw + (size_t)(t0 - CONV_TAPS + i) * a.raw_stride + col, win[i]);
+                for (int i = 0; i < CONV_TAPS; ++i)
+                    ld8(raw + (size_t)(t0 - CONV_TAPS + i) * a.raw_stride + col, wn[i]);
+            }
         }
-    } else {
+        unpack_taps(wp, w);
 #pragma unroll
-        for (int i = 0; i < CONV_W; ++i) zero8(w[i]);
+        for (int i = 0; i < CONV_TAPS; ++i)
 #pragma unroll
-        for (int i = 0; i < CONV_TAPS; ++i) zero8(win[i]);
+            for (int e = 0; e < LANE_CH; ++e) win[i][e] = el(wn[i], e);
     }
     for (int j0 = 0; j0 < cnt; j0 += PRO_PREFETCH) {
         Pack8<T> x[PRO_PREFETCH];
@@ -99,19 +103,20 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
         }
     }
     if (tile == 0 && so >= 0 && live) {
-        // the last W-1 raw inputs of the sequence (from the old state where it is shorter)
+        // the last W-1 raw inputs of the sequence, from the old state where it
+        // is shorter (this CTA is the slot's only reader and writer, and it has
+        // not written it yet)
         const int len = eos - bos;
 #pragma unroll
         for (int i = 0; i < CONV_TAPS; ++i) {
             const int p = len - CONV_TAPS + i;   // position relative to the sequence start
-            Pack8<T> v = init[0];
-            if (p >= 0) {
+            Pack8<T> v;
+            if (p >= 0)
                 ld8(raw + (size_t)(bos + p) * a.raw_stride + col, v);
-            } else {
-#pragma unroll
-                for (int m = 1; m < CONV_TAPS; ++m)
-                    if (m == p + CONV_TAPS) v = init[m];
-            }
+            else if (si >= 0)
+                ld8(cs + conv_state_idx(si, p + CONV_TAPS, s, a.H, h, c0), v);
+            else
+                zero8(v);
             st8(cs + conv_state_idx(so, i, s, a.H, h, c0), v);
         }
     }
@@ -121,19 +126,19 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
 template <typename T>
 __global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormArgs a) {
     const int lane = threadIdx.x & 31, c0 = (lane & 15) * LANE_CH;
-    const size_t rows = (size_t)a.tokens * a.H;
+    const unsigned rows = (unsigned)a.tokens * (unsigned)a.H;   // < 2^31 (checked on the host)
     float wn[LANE_CH];
     load8((const T *)a.w_norm + c0, wn);
-    const size_t nwarps = (size_t)gridDim.x * (CTA_THREADS / 32);
-    for (size_t pair = (size_t)blockIdx.x * (CTA_THREADS / 32) + (threadIdx.x >> 5); pair * 2 < rows;
+    const unsigned nwarps = gridDim.x * (CTA_THREADS / 32);
+    for (unsigned pair = blockIdx.x * (CTA_THREADS / 32) + (threadIdx.x >> 5); pair * 2 < rows;
          pair += nwarps) {
-        const size_t row = pair * 2 + (lane >> 4);
+        const unsigned row = pair * 2 + (lane >> 4);
         const bool live = row < rows;
         float o[LANE_CH], g[LANE_CH];
         if (live) {
-            const size_t t = row / a.H, h = row - t * a.H;
-            load8((const T *)a.o + t * a.o_token_stride + h * a.o_head_stride + c0, o);
-            load8((const T *)a.gate + row * VD + c0, g);
+            const unsigned t = row / (unsigned)a.H, h = row - t * (unsigned)a.H;
+            load8((const T *)a.o + (size_t)t * a.o_token_stride + (size_t)h * a.o_head_stride + c0, o);
+            load8((const T *)a.gate + (size_t)row * VD + c0, g);
         } else {
 #pragma unroll
             for (int e = 0; e < LANE_CH; ++e) o[e] = g[e] = 0.f;
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormAr
         float y[LANE_CH];
 #pragma unroll
         for (int e = 0; e < LANE_CH; ++e) y[e] = gated_norm(o[e], f, wn[e], g[e]);
-        if (live) store8((T *)a.out + row * VD + c0, y);
+        if (live) store8((T *)a.out + (size_t)row * VD + c0, y);
     }
 }
 
