@@ -625,12 +625,22 @@ class OracleVarlen:
 CSRC = os.path.join(ROOT, "kda_state_gb300", "csrc")
 
 
+def _device_headers(name, seen):
+    """The local device headers (.cuh) a source includes, depth first, in order."""
+    for line in open(os.path.join(CSRC, name)):
+        m = re.match(r'\s*#include\s+"([^"/]+\.cuh)"', line)
+        if m and m.group(1) not in seen:
+            seen.append(m.group(1))
+            _device_headers(m.group(1), seen)
+    return seen
+
+
 def source_sha1(kernel_file):
     """First 12 hex digits of the sha1 over a kernel's source file followed by
-    the shared device header it includes (the hash the profile summaries
-    record as source_sha1)."""
+    the device headers it includes (the hash the profile summaries record as
+    source_sha1)."""
     h = hashlib.sha1()
-    for f in (kernel_file, "kda_common.cuh"):
+    for f in [kernel_file] + _device_headers(kernel_file, []):
         h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -843,6 +853,8 @@ def main():
                 "fused_kernel_us": df["fused_ms"] * 1e3,
                 "fused_kernel_GBps": df["fused_bytes"] / (df["fused_ms"] / 1e3) / 1e9,
                 "fused_kernel_frac": df["fused_bytes"] / (df["fused_ms"] / 1e3) / 1e9 / hbm,
+                "fused_kernel_traffic": profile_traffic("kda_decode_fused.cu",
+                                                        "decode_fused_kernel.decode_fused.md"),
             }
         except Exception as e:  # noqa: BLE001
             also["decode_fused"] = {"error": repr(e)}
@@ -857,6 +869,11 @@ def main():
                 "prefill_us": pf["prefill_ms"] * 1e3,
                 "norm_us": pf["norm_ms"] * 1e3,
                 "norm_frac": pf["norm_bytes"] / (pf["norm_ms"] / 1e3) / 1e9 / hbm,
+                "prologue_traffic": profile_traffic(
+                    "kda_prologue.cu", "conv_prologue_kernel_gated_rmsnorm_kernel.prefill_fused.md"),
+                "norm_traffic": profile_traffic(
+                    "kda_prologue.cu", "conv_prologue_kernel_gated_rmsnorm_kernel.prefill_fused.md",
+                    "norm_dram_bytes_per_launch"),
             }
         except Exception as e:  # noqa: BLE001
             also["prefill_fused_path"] = {"error": repr(e)}
