@@ -153,3 +153,30 @@ def test_prefill_checkpoints_bad_slot(dtype):
     assert_close(pool[1:3], S_ref[1:3], dtype, "final states")
     assert_close(pool[6], ck_ref[2, 0], dtype, "checkpoint")
     assert torch.equal(pool[7], before[7]) and torch.equal(pool[3:5], before[3:5])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_prefill_checkpoints_none_due(dtype):
+    """An interval longer than every sequence makes no checkpoint: the call
+    equals the plain prefill and leaves every checkpoint slot untouched."""
+    lengths = [100, 0, 255]
+    H, N = 2, 3
+    g = gen.make_gen(23)
+    cu = gen.cu_seqlens(lengths)
+    x = gen.token_inputs(int(cu[-1]), H, dtype, g)
+    xd = _dev(x)
+    pool = canary_fill(torch.empty(2 * N + 2, H, KD, VD, device=DEV))
+    before = pool.clone()
+    init = torch.full((N,), -1, dtype=torch.int32, device=DEV)
+    out = torch.arange(N, 2 * N, dtype=torch.int32, device=DEV)
+    slots = torch.tensor([[6, 7]] * N, dtype=torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = kda().kda_chunk_prefill_checkpoints(xd["q"], xd["k"], xd["v"], xd["gk"], xd["beta"],
+                                            cu.to(DEV), cu, pool, init, out, 256, slots.to(DEV),
+                                            dev_err=err)
+    pool_p = before.clone()
+    o_p = _plain(xd, cu, pool_p, init, out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o, o_p) and torch.equal(pool, pool_p)
+    assert torch.equal(pool[6:], before[6:])

@@ -140,3 +140,24 @@ def test_ragged_verify_bad_offsets(dtype):
         assert_close(o[sl], ref, dtype, "request %d" % [0, 3][b])
     assert not o[3:12].any() and not o[14:].any()
     assert not ring.k[[1, 2, 4]].any()
+
+
+def test_ragged_verify_all_empty():
+    """Every request trims its window to zero drafts: nothing is read or
+    written, no error is raised."""
+    H, S = 2, 4
+    g = gen.make_gen(62)
+    pool = gen.checkpoint((S, H, KD, VD), g).to(DEV)
+    before = pool.clone()
+    ring = kda().make_ring(S, 16, H, torch.bfloat16, DEV)
+    cu = torch.zeros(4, dtype=torch.int32, device=DEV)
+    empty = torch.empty(0, H, KD, dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda().kda_verify_store_inputs_ragged(empty, empty, empty, empty,
+                                         torch.empty(0, H, dtype=torch.bfloat16, device=DEV), cu, 8,
+                                         torch.tensor([0, 1, 2], dtype=torch.int32, device=DEV),
+                                         pool, ring, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(pool, before)
+    assert not ring.k.any() and not ring.decay.any()

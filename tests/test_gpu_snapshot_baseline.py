@@ -35,7 +35,7 @@ def _dev(x):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
-@pytest.mark.parametrize("G", [3, 8])
+@pytest.mark.parametrize("G", [1, 3, 8])
 def test_snapshot_verify_commit(dtype, G):
     g = gen.make_gen(71 + G)
     B, H, L, S = 5, 2, 2, 12
