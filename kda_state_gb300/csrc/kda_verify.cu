@@ -4,6 +4,7 @@
 // (lmsys.org), "ReplaySSM: raw-input replay for the KDA state": verify reads the
 // committed checkpoint, never writes it, and stores each draft step's
 // (k, v, gate, beta) into a per-slot ring.
+#include "kda_async.cuh"
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -93,7 +94,11 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
 // column 16w + (l & 15) and rows 64 (l >> 4) .. + 63.
 constexpr int XS = KD + 4;   // padded row stride of W and q . E (conflict-free fragment loads)
 
-template <int GM>
+constexpr int HS = KD + 8;   // row stride of the staged h0: conflict-free B-fragment loads
+
+// H0S: h0 staged in shared memory by bulk copies (the tensor path), one row
+// of 512 bytes per copy into rows HS floats apart.
+template <int GM, bool H0S>
 struct VerifyBlockSmem {
     float kg[GM][KD];   // k . E
     float kn[GM][KD];   // k / E
@@ -104,12 +109,16 @@ struct VerifyBlockSmem {
     float akk[GM][GM], aqk[GM][GM], tb[GM][GM];
     float beta[GM];
     int fallback;
+    int h0_ok;
+    alignas(8) uint64_t bar;
+    alignas(16) float h0s[H0S ? KD : 1][HS];
 };
 
 template <typename T, int GM>
 __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    VerifyBlockSmem<GM> &sm = *reinterpret_cast<VerifyBlockSmem<GM> *>(smem);
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
+    VerifyBlockSmem<GM, TENSOR> &sm = *reinterpret_cast<VerifyBlockSmem<GM, TENSOR> *>(smem);
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit - b * a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -125,23 +134,21 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         return;
     }
     if (G == 0) return;
-    // h0 into registers (read-only).  Tensor path (bf16 inputs, G <= 8): the B
-    // fragments of m16n8k8 for this warp's 16 columns, as tf32.  CUDA-core path:
-    // column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
-    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
+    // h0 (read-only).  Tensor path (bf16 inputs, G <= 8): 128 bulk copies, one
+    // row each, land it in shared memory while the draft is staged and its
+    // matrices formed; the m16n8k8 B fragments are read from there.  CUDA-core
+    // path: registers, column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
     const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS;
     const int col = 16 * warp + (lane & 15), hr = lane >> 4;
     const int g = lane >> 2, t4 = lane & 3;
-    float s[64];
+    float s[TENSOR ? 1 : 64];
+    const uint32_t bar = shared_addr(&sm.bar);
     if (TENSOR) {
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    s[(ks * 2 + nt) * 2 + e] =
-                        __ldg(S0 + (size_t)(8 * ks + t4 + 4 * e) * VD + 16 * warp + 8 * nt + g);
+        if (tid == 0) {
+            barrier_init(bar, 1);
+            barrier_expect(bar, (uint32_t)(sizeof(float) * STATE_ELEMS));
+        }
+        __syncthreads();   // the copies below (issued after the draft's loads) complete on bar
     } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)(64 * hr + i) * VD + col);
@@ -164,6 +171,9 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                 gr[i] = ((const T *)a.gk)[tok * KD + c];
             }
         }
+        // h0 streams in behind the draft (8 KB), which the Gram, the solve and
+        // W / U~ need first; only the final product waits for h0
+        if (TENSOR) bulk_copy(sm.h0s[c], S0 + (size_t)c * VD, VD * sizeof(float), bar);
         float E = 1.f;
         bool tiny = false;
 #pragma unroll
@@ -210,34 +220,57 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
     __syncthreads();
     if (sm.fallback) {
         // The records above are the same ones the recurrent form stores; it
-        // rewrites them identically.
+        // rewrites them identically.  Its scratch reuses this shared memory,
+        // so the h0 copies must have landed first.
+        if (TENSOR && tid == 0) sm.h0_ok = barrier_wait(bar, 0);
         __syncthreads();
+        if (TENSOR && !sm.h0_ok) {
+            if (tid == 0) report(a.err, DEVERR_TIMEOUT);
+            return;
+        }
         verify_unit_recurrent<T>(a, b, h, slot, tok0, G, smem);
         return;
     }
-    // Gram entries: pair p -> (r, j); pairs [0, G(G-1)/2) are A, the rest Aqk
-    const int nkk = G * (G - 1) / 2, npairs = nkk + G * (G + 1) / 2;
-    for (int pidx = warp; pidx < npairs; pidx += CTA_WARPS) {
-        int r, j;
-        const bool is_kk = pidx < nkk;
-        {
-            int q = is_kk ? pidx : pidx - nkk;   // enumerate rows of a lower triangle
-            r = is_kk ? 1 : 0;
-            while (q >= (is_kk ? r : r + 1)) { q -= (is_kk ? r : r + 1); ++r; }
-            j = q;
-        }
-        const float4 x = reinterpret_cast<const float4 *>(is_kk ? sm.kg[r] : sm.qg[r])[lane];
-        const float4 y = reinterpret_cast<const float4 *>(sm.kn[j])[lane];
-        float d = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+    // Gram rows: warp w takes draft rows r = w, w + 8, ...; each lane holds 4
+    // channels of k_r E_r and q_r E_r and accumulates the row's products with
+    // every k_j / E_j, then one butterfly per product (independent, so they
+    // overlap).  A[r][j] = b_r <k_r E_r, k_j / E_j> (j < r), Aqk[r][j] =
+    // <q_r E_r, k_j / E_j> (j <= r).
+    for (int r = warp; r < G; r += CTA_WARPS) {
+        const float4 kr4 = reinterpret_cast<const float4 *>(sm.kg[r])[lane];
+        const float4 qr4 = reinterpret_cast<const float4 *>(sm.qg[r])[lane];
+        float dk[GM], dq[GM];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        for (int j = 0; j < GM; ++j) {
+            dk[j] = 0.f;
+            dq[j] = 0.f;
+            if (j <= r) {
+                const float4 y = reinterpret_cast<const float4 *>(sm.kn[j])[lane];
+                dk[j] = kr4.x * y.x + kr4.y * y.y + kr4.z * y.z + kr4.w * y.w;
+                dq[j] = qr4.x * y.x + qr4.y * y.y + qr4.z * y.z + qr4.w * y.w;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                dk[j] += __shfl_xor_sync(0xffffffffu, dk[j], off);
+                dq[j] += __shfl_xor_sync(0xffffffffu, dq[j], off);
+            }
+        }
         if (lane == 0) {
-            if (is_kk) sm.akk[r][j] = d * sm.beta[r];
-            else sm.aqk[r][j] = d;
+            const float br = sm.beta[r];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                if (j < r) sm.akk[r][j] = dk[j] * br;
+                if (j <= r) sm.aqk[r][j] = dq[j];
+            }
         }
     }
     __syncthreads();
-    // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b)
+    // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b).
+    // Each row's entries of A are loaded before its FMA chain (they do not
+    // depend on x), so the loads overlap the previous rows' chains.
     if (warp == 0 && lane < G) {
         const int cc = lane;
         float x[GM];
@@ -245,15 +278,19 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         for (int r = 0; r < GM; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
         for (int r = 1; r < GM; ++r) {
-            if (r < G && r > cc) {
-                float acc = 0.f;
+            float ar[GM];
 #pragma unroll
-                for (int j = 0; j < GM; ++j)
-                    if (j < r) acc = fmaf(sm.akk[r][j], x[j], acc);
-                x[r] = -acc;
-            }
+            for (int j = 0; j < GM; ++j) ar[j] = (j < r) ? sm.akk[r][j] : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < GM; ++j)
+                if (j < r) acc = fmaf(ar[j], x[j], acc);
+            if (r < G && r > cc) x[r] = -acc;
         }
-        for (int r = 0; r < G; ++r) sm.tb[r][cc] = (r >= cc) ? x[r] * sm.beta[cc] : 0.f;
+        const float bc = sm.beta[cc];
+#pragma unroll
+        for (int r = 0; r < GM; ++r)
+            if (r < G) sm.tb[r][cc] = (r >= cc) ? x[r] * bc : 0.f;
     }
     __syncthreads();
     // W = T Diag(b) (K . E) and U~ = T Diag(b) V, one column per thread
@@ -272,8 +309,13 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
             }
         }
     }
+    if (TENSOR && tid == 0) sm.h0_ok = barrier_wait(bar, 0);   // h0 has landed
     __syncthreads();
     if (TENSOR) {
+        if (!sm.h0_ok) {
+            if (tid == 0) report(a.err, DEVERR_TIMEOUT);
+            return;
+        }
         // [W; Q . E] (16 x 128) h0 (128 x 16 columns of this warp): 16 k-steps x
         // 2 n-tiles of m16n8k8 TF32.  Row g of the result is W row g (c[.][0..1])
         // and (Q . E) row g (c[.][2..3]) at columns 16w + 8nt + 2t4 (+1).
@@ -285,7 +327,8 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                                     tf32_bits(sm.w[g][k + 4]), tf32_bits(sm.qg[g][k + 4])};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t bf[2] = {tf32_bits(s[(ks * 2 + nt) * 2]), tf32_bits(s[(ks * 2 + nt) * 2 + 1])};
+                const float *hb = &sm.h0s[8 * ks + t4][16 * warp + 8 * nt + g];
+                const uint32_t bf[2] = {tf32_bits(hb[0]), tf32_bits(hb[4 * HS])};
                 mma16n8k8_tf32(c[nt], af, bf);
             }
         }
@@ -359,7 +402,9 @@ template <typename T, int GM>
 cudaError_t launch_verify_block(const VerifyArgs &a, cudaStream_t s) {
     const unsigned grid = (unsigned)a.B * (unsigned)a.H;
     const size_t rec = sizeof(Reduce) + (size_t)a.G * sizeof(TokenIn);   // fallback's needs
-    const size_t smem = sizeof(VerifyBlockSmem<GM>) > rec ? sizeof(VerifyBlockSmem<GM>) : rec;
+    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
+    const size_t blk = sizeof(VerifyBlockSmem<GM, TENSOR>);
+    const size_t smem = blk > rec ? blk : rec;
     cudaError_t e = set_smem(verify_block_kernel<T, GM>, smem);
     if (e != cudaSuccess) return e;
     verify_block_kernel<T, GM><<<grid, CTA_THREADS, smem, s>>>(a);
