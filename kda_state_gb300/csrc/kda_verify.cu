@@ -114,6 +114,144 @@ struct VerifyBlockSmem {
     alignas(16) float h0s[H0S ? KD : 1][HS];
 };
 
+// ---------------------------------------------------------------------------
+// Block-form phases of one unit.  Each is followed by a block barrier in the
+// caller.
+// ---------------------------------------------------------------------------
+template <int GM, bool H0S>
+__device__ __forceinline__ void block_gram(VerifyBlockSmem<GM, H0S> &sm, int G, int warp, int lane) {
+    // Gram rows: warp w takes draft rows r = w, w + 8, ...; each lane holds 4
+    // channels of k_r E_r and q_r E_r and accumulates the row's products with
+    // every k_j / E_j, then one butterfly per product (independent, so they
+    // overlap).  A[r][j] = b_r <k_r E_r, k_j / E_j> (j < r), Aqk[r][j] =
+    // <q_r E_r, k_j / E_j> (j <= r).
+    for (int r = warp; r < G; r += CTA_WARPS) {
+        const float4 kr4 = reinterpret_cast<const float4 *>(sm.kg[r])[lane];
+        const float4 qr4 = reinterpret_cast<const float4 *>(sm.qg[r])[lane];
+        float dk[GM], dq[GM];
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+            dk[j] = 0.f;
+            dq[j] = 0.f;
+            if (j <= r) {
+                const float4 y = reinterpret_cast<const float4 *>(sm.kn[j])[lane];
+                dk[j] = kr4.x * y.x + kr4.y * y.y + kr4.z * y.z + kr4.w * y.w;
+                dq[j] = qr4.x * y.x + qr4.y * y.y + qr4.z * y.z + qr4.w * y.w;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                dk[j] += __shfl_xor_sync(0xffffffffu, dk[j], off);
+                dq[j] += __shfl_xor_sync(0xffffffffu, dq[j], off);
+            }
+        }
+        if (lane == 0) {
+            const float br = sm.beta[r];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                if (j < r) sm.akk[r][j] = dk[j] * br;
+                if (j <= r) sm.aqk[r][j] = dq[j];
+            }
+        }
+    }
+}
+
+template <int GM, bool H0S>
+__device__ __forceinline__ void block_solve(VerifyBlockSmem<GM, H0S> &sm, int G, int warp, int lane) {
+    // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b).
+    // Each row's entries of A are loaded before its FMA chain (they do not
+    // depend on x), so the loads overlap the previous rows' chains.
+    if (warp == 0 && lane < G) {
+        const int cc = lane;
+        float x[GM];
+#pragma unroll
+        for (int r = 0; r < GM; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < GM; ++r) {
+            float ar[GM];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) ar[j] = (j < r) ? sm.akk[r][j] : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < GM; ++j)
+                if (j < r) acc = fmaf(ar[j], x[j], acc);
+            if (r < G && r > cc) x[r] = -acc;
+        }
+        const float bc = sm.beta[cc];
+#pragma unroll
+        for (int r = 0; r < GM; ++r)
+            if (r < G) sm.tb[r][cc] = (r >= cc) ? x[r] * bc : 0.f;
+    }
+}
+
+template <int GM, bool H0S>
+__device__ __forceinline__ void block_wu(VerifyBlockSmem<GM, H0S> &sm, int G, int tid) {
+    // W = T Diag(b) (K . E) and U~ = T Diag(b) V, one column per thread
+    const int c = tid & (KD - 1);
+    const bool do_w = tid < KD;
+    for (int r = 0; r < GM; ++r) {
+        float acc = 0.f;
+        if (r < G)
+            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
+        if (do_w) {
+            sm.w[r][c] = acc;
+            if (r >= G) sm.qg[r][c] = 0.f;
+        } else {
+            sm.ut[r][c] = acc;
+        }
+    }
+}
+
+// [W; Q . E] h0 on warp-level TF32 MMAs with h0 from shared memory, then
+// U = U~ - W h0 and O = (Q . E) h0 + Aqk U; writes the G output rows.
+template <typename T>
+__device__ __forceinline__ void block_tensor_out(VerifyBlockSmem<8, true> &sm, const VerifyArgs &a,
+                                                 size_t tok0, int G, int h, int warp, int lane) {
+    constexpr int GM = 8;
+    const int g = lane >> 2, t4 = lane & 3;
+    // [W; Q . E] (16 x 128) h0 (128 x 16 columns of this warp): 16 k-steps x
+    // 2 n-tiles of m16n8k8 TF32.  Row g of the result is W row g (c[.][0..1])
+    // and (Q . E) row g (c[.][2..3]) at columns 16w + 8nt + 2t4 (+1).
+    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+        const int k = 8 * ks + t4;
+        const uint32_t af[4] = {tf32_bits(sm.w[g][k]), tf32_bits(sm.qg[g][k]),
+                                tf32_bits(sm.w[g][k + 4]), tf32_bits(sm.qg[g][k + 4])};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float *hb = &sm.h0s[8 * ks + t4][16 * warp + 8 * nt + g];
+            const uint32_t bf[2] = {tf32_bits(hb[0]), tf32_bits(hb[4 * HS])};
+            mma16n8k8_tf32(c[nt], af, bf);
+        }
+    }
+    // U = U~ - W h0 for row g; O = (Q . E) h0 + Aqk U, U rows from the lanes
+    // holding them (lane 4j + t4)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c0 = 16 * warp + 8 * nt + 2 * t4;
+        const float u0 = sm.ut[g][c0] - c[nt][0], u1 = sm.ut[g][c0 + 1] - c[nt][1];
+        float o0 = c[nt][2], o1 = c[nt][3];
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+            const float uj0 = __shfl_sync(0xffffffffu, u0, 4 * j + t4);
+            const float uj1 = __shfl_sync(0xffffffffu, u1, 4 * j + t4);
+            if (j <= g && j < G) {
+                const float aq = sm.aqk[g][j];
+                o0 = fmaf(aq, uj0, o0);
+                o1 = fmaf(aq, uj1, o1);
+            }
+        }
+        if (g < G) {
+            T *dst = (T *)a.o + ((tok0 + g) * a.H + h) * VD + c0;
+            dst[0] = from_f<T>(a.scale * o0);
+            dst[1] = from_f<T>(a.scale * o1);
+        }
+    }
+}
+
 template <typename T, int GM>
 __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -143,18 +281,18 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
     const int g = lane >> 2, t4 = lane & 3;
     float s[TENSOR ? 1 : 64];
     const uint32_t bar = shared_addr(&sm.bar);
-    if (TENSOR) {
-        if (tid == 0) {
+    if (tid == 0) {
+        sm.fallback = 0;   // set by the staging below, after the barrier
+        if (TENSOR) {
             barrier_init(bar, 1);
             barrier_expect(bar, (uint32_t)(sizeof(float) * STATE_ELEMS));
         }
-        __syncthreads();   // the copies below (issued after the draft's loads) complete on bar
-    } else {
+    }
+    if (!TENSOR) {
 #pragma unroll
         for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)(64 * hr + i) * VD + col);
     }
-
-    if (tid == 0) sm.fallback = 0;
+    __syncthreads();   // the reset, and the barrier the h0 copies (issued after the draft's loads) complete on
     const int base = a.ring_base ? a.ring_base[b] : 0;
     const int mask = a.ring_len - 1;
     // stage the draft, store the records; running decay products per channel.
@@ -231,130 +369,19 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         verify_unit_recurrent<T>(a, b, h, slot, tok0, G, smem);
         return;
     }
-    // Gram rows: warp w takes draft rows r = w, w + 8, ...; each lane holds 4
-    // channels of k_r E_r and q_r E_r and accumulates the row's products with
-    // every k_j / E_j, then one butterfly per product (independent, so they
-    // overlap).  A[r][j] = b_r <k_r E_r, k_j / E_j> (j < r), Aqk[r][j] =
-    // <q_r E_r, k_j / E_j> (j <= r).
-    for (int r = warp; r < G; r += CTA_WARPS) {
-        const float4 kr4 = reinterpret_cast<const float4 *>(sm.kg[r])[lane];
-        const float4 qr4 = reinterpret_cast<const float4 *>(sm.qg[r])[lane];
-        float dk[GM], dq[GM];
-#pragma unroll
-        for (int j = 0; j < GM; ++j) {
-            dk[j] = 0.f;
-            dq[j] = 0.f;
-            if (j <= r) {
-                const float4 y = reinterpret_cast<const float4 *>(sm.kn[j])[lane];
-                dk[j] = kr4.x * y.x + kr4.y * y.y + kr4.z * y.z + kr4.w * y.w;
-                dq[j] = qr4.x * y.x + qr4.y * y.y + qr4.z * y.z + qr4.w * y.w;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int j = 0; j < GM; ++j) {
-                dk[j] += __shfl_xor_sync(0xffffffffu, dk[j], off);
-                dq[j] += __shfl_xor_sync(0xffffffffu, dq[j], off);
-            }
-        }
-        if (lane == 0) {
-            const float br = sm.beta[r];
-#pragma unroll
-            for (int j = 0; j < GM; ++j) {
-                if (j < r) sm.akk[r][j] = dk[j] * br;
-                if (j <= r) sm.aqk[r][j] = dq[j];
-            }
-        }
-    }
+    block_gram(sm, G, warp, lane);
     __syncthreads();
-    // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b).
-    // Each row's entries of A are loaded before its FMA chain (they do not
-    // depend on x), so the loads overlap the previous rows' chains.
-    if (warp == 0 && lane < G) {
-        const int cc = lane;
-        float x[GM];
-#pragma unroll
-        for (int r = 0; r < GM; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 1; r < GM; ++r) {
-            float ar[GM];
-#pragma unroll
-            for (int j = 0; j < GM; ++j) ar[j] = (j < r) ? sm.akk[r][j] : 0.f;
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < GM; ++j)
-                if (j < r) acc = fmaf(ar[j], x[j], acc);
-            if (r < G && r > cc) x[r] = -acc;
-        }
-        const float bc = sm.beta[cc];
-#pragma unroll
-        for (int r = 0; r < GM; ++r)
-            if (r < G) sm.tb[r][cc] = (r >= cc) ? x[r] * bc : 0.f;
-    }
+    block_solve(sm, G, warp, lane);
     __syncthreads();
-    // W = T Diag(b) (K . E) and U~ = T Diag(b) V, one column per thread
-    {
-        const int c = tid & (KD - 1);
-        const bool do_w = tid < KD;
-        for (int r = 0; r < GM; ++r) {
-            float acc = 0.f;
-            if (r < G)
-                for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
-            if (do_w) {
-                sm.w[r][c] = acc;
-                if (r >= G) sm.qg[r][c] = 0.f;
-            } else {
-                sm.ut[r][c] = acc;
-            }
-        }
-    }
+    block_wu(sm, G, tid);
     if (TENSOR && tid == 0) sm.h0_ok = barrier_wait(bar, 0);   // h0 has landed
     __syncthreads();
-    if (TENSOR) {
+    if constexpr (TENSOR) {
         if (!sm.h0_ok) {
             if (tid == 0) report(a.err, DEVERR_TIMEOUT);
             return;
         }
-        // [W; Q . E] (16 x 128) h0 (128 x 16 columns of this warp): 16 k-steps x
-        // 2 n-tiles of m16n8k8 TF32.  Row g of the result is W row g (c[.][0..1])
-        // and (Q . E) row g (c[.][2..3]) at columns 16w + 8nt + 2t4 (+1).
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-            const int k = 8 * ks + t4;
-            const uint32_t af[4] = {tf32_bits(sm.w[g][k]), tf32_bits(sm.qg[g][k]),
-                                    tf32_bits(sm.w[g][k + 4]), tf32_bits(sm.qg[g][k + 4])};
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float *hb = &sm.h0s[8 * ks + t4][16 * warp + 8 * nt + g];
-                const uint32_t bf[2] = {tf32_bits(hb[0]), tf32_bits(hb[4 * HS])};
-                mma16n8k8_tf32(c[nt], af, bf);
-            }
-        }
-        // U = U~ - W h0 for row g; O = (Q . E) h0 + Aqk U, U rows from the lanes
-        // holding them (lane 4j + t4)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int c0 = 16 * warp + 8 * nt + 2 * t4;
-            const float u0 = sm.ut[g][c0] - c[nt][0], u1 = sm.ut[g][c0 + 1] - c[nt][1];
-            float o0 = c[nt][2], o1 = c[nt][3];
-#pragma unroll
-            for (int j = 0; j < GM; ++j) {
-                const float uj0 = __shfl_sync(0xffffffffu, u0, 4 * j + t4);
-                const float uj1 = __shfl_sync(0xffffffffu, u1, 4 * j + t4);
-                if (j <= g && j < G) {
-                    const float aq = sm.aqk[g][j];
-                    o0 = fmaf(aq, uj0, o0);
-                    o1 = fmaf(aq, uj1, o1);
-                }
-            }
-            if (g < G) {
-                T *dst = (T *)a.o + ((tok0 + g) * a.H + h) * VD + c0;
-                dst[0] = from_f<T>(a.scale * o0);
-                dst[1] = from_f<T>(a.scale * o1);
-            }
-        }
+        block_tensor_out<T>(sm, a, tok0, G, h, warp, lane);
         return;
     }
     // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
@@ -411,6 +438,8 @@ cudaError_t launch_verify_block(const VerifyArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The recurrent fallback's scratch (Reduce + G TokenIn) must stay below h0s,
+// where copies may be in flight.
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s) {
     const bool bf = a.dt == KDA_DTYPE_BF16;
     if (a.G <= 8)
