@@ -100,6 +100,7 @@ enum { FLAG_TIMEOUT = 1, FLAG_RANGE = 2 };
 
 struct Params {
     CUtensorMap tq, tk, tg, tv;
+    CUtensorMap to;   // o: boxes of 32 channels x 1 head x 32 tokens, 64-byte swizzle
     int N, T_total, H, num_slots, lpt;
     const __nv_bfloat16 *beta;
     const int32_t *cu;
@@ -159,6 +160,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+// Bulk tensor store of a shared-memory box; completes in this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -364,6 +381,51 @@ __device__ __forceinline__ void solve_block_column(const float *As, float *Ts, f
     }
 }
 
+// O of a chunk, from rows 64..127 of TMEM columns 128..255: this warp's lane
+// quarter lq (2 or 3) and columns 32 cq .. 32 cq + 31, scaled, rounded to bf16
+// and stored for the chunk's first L tokens (the chunk starts at token t0).
+__device__ __forceinline__ void store_o(const Params &p, uint32_t tmem, int lq, int cq, int lane, int t0,
+                                        int L, int h) {
+    uint32_t r[32];
+    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+    tmem_wait_ld();
+    const int row = 32 * (lq - 2) + lane;
+    if (row < L) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + row) * p.H + h) * VD + 32 * cq);
+        const float sc = p.scale;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float *f = reinterpret_cast<const float *>(r + 8 * j);
+            dst[j] = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
+                                pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
+        }
+    }
+}
+
+// O of a full chunk by tensor store: the warp stages its 32 tokens x 32
+// channels as one 64-byte-swizzled box (2 KB) in rows 0..63 of the [-W; Q~]
+// tile, free until the -W read-out, and lane 0 stores it; lane 0 waits for the
+// box to be read (tma_store_wait_read) before that tile is written again.
+__device__ __forceinline__ void store_o_tma(const Params &p, uint8_t *sm, uint32_t sbase, uint32_t tmem,
+                                            int lq, int cq, int lane, int t0, int h) {
+    uint32_t r[32];
+    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+    tmem_wait_ld();
+    const int box = 4 * (lq - 2) + cq;
+    const uint32_t stage = OP_A3 + (box >> 2) * 16384 + (box & 3) * 2048;
+    const float sc = p.scale;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float *f = reinterpret_cast<const float *>(r + 8 * j);
+        *reinterpret_cast<uint4 *>(sm + stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
+                       pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) tma_store_3d(&p.to, sbase + stage, 32 * cq, h, t0 + 32 * (lq - 2));
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -453,59 +515,78 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     for (int j = 0; j < 4; ++j) store_f16(sm + OP_S, chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
 
     const float LOG2E = 1.4426950408889634f;
-    // beta of the chunk about to be processed, loaded one chunk ahead
-    float beta_next = 0.f;
-    if (tid < C && nchunks > 0 && tid < min(C, eos - bos))
-        beta_next = __bfloat162float(p.beta[(size_t)(bos + tid) * p.H + h]);
+    // beta of the chunk about to be processed, loaded one chunk ahead.  The raw
+    // bf16 bits stay in a register and are converted only when the next chunk
+    // stores them, so no thread waits for this load inside the chunk; a token
+    // past the sequence loads its sequence's first beta and stores 0.
+    const unsigned short *beta_bits = reinterpret_cast<const unsigned short *>(p.beta);
+    unsigned short beta_raw = 0;
+    bool beta_ok = false;
+    if (tid < C && nchunks > 0) {
+        beta_ok = tid < eos - bos;
+        beta_raw = __ldg(beta_bits + (size_t)(beta_ok ? bos + tid : bos) * p.H + h);
+    }
     constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 2);
     constexpr uint32_t ID_G2 = idesc(128, 128, 0, 1, 1);
     constexpr uint32_t ID_G3 = idesc(128, 128, 0, 1, 0);
     constexpr uint32_t ID_G4A = idesc(128, 128, 0, 1, 0);
     constexpr uint32_t ID_G4B = idesc(128, 128, 1, 1, 0);
-    bool aborted = false;
-    for (int c = 0; c < nchunks; ++c) {
+    // This thread's share of the raw q, k, gk tiles, taken into registers while
+    // the previous chunk's G4 runs (for chunk 0: here).  Warp w owns key
+    // channels 8w .. 8w+7; lane l owns rows 2l and 2l + 1, taken in the order
+    // rA, rB: lanes with bit 2 set take the odd row first, so that the 8 lanes
+    // of each quarter-warp cover all 8 positions of the 128-byte swizzle in
+    // every load and in every store of the prep phase.
+    uint4 wqA, wqB, wkA, wkB, wgA, wgB;
+    auto load_raw = [&]() {
+        const int ch = 8 * warp, sw = (lane >> 2) & 1;
+        const int rA = 2 * lane + sw, rB = 2 * lane + 1 - sw;
+        wqA = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(rA, ch, 64));
+        wqB = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(rB, ch, 64));
+        wkA = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(rA, ch, 64));
+        wkB = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(rB, ch, 64));
+        wgA = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(rA, ch, 64));
+        wgB = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(rB, ch, 64));
+    };
+    if (nchunks > 0 && !mbar_wait(bar_qkg, 0)) atomicOr(flags, FLAG_TIMEOUT);
+    load_raw();
+    __syncthreads();   // the raw tiles may now be overwritten
+    bool aborted = (*flags & FLAG_TIMEOUT) != 0;
+    for (int c = 0; c < nchunks && !aborted; ++c) {
         const int t0 = bos + c * C;
         const int L = min(C, eos - t0);
         const uint32_t par = (uint32_t)(c & 1);
 
-        // (1) raw q, k, gk have landed: take this thread's share into registers
-        if (!mbar_wait(bar_qkg, par)) atomicOr(flags, FLAG_TIMEOUT);
+        // (1) beta of this chunk into shared memory; the next chunk's is loaded
         if (tid < C) {
-            beta_s[tid] = beta_next;
+            beta_s[tid] = beta_ok ? __uint_as_float((uint32_t)beta_raw << 16) : 0.f;
             const int tn = t0 + C + tid;
-            beta_next = (c + 1 < nchunks && tn < eos) ? __bfloat162float(p.beta[(size_t)tn * p.H + h]) : 0.f;
+            beta_ok = c + 1 < nchunks && tn < eos;
+            beta_raw = __ldg(beta_bits + (size_t)(beta_ok ? tn : bos) * p.H + h);
         }
-        // warp w owns key channels 8w .. 8w+7; lane l owns rows 2l and 2l + 1
-        const int ch = 8 * warp;
-        const int r0 = 2 * lane, r1 = 2 * lane + 1;
-        const uint4 wq0 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r0, ch, 64));
-        const uint4 wq1 = *reinterpret_cast<const uint4 *>(sm + RAW_Q + chunk_off(r1, ch, 64));
-        const uint4 wk0 = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(r0, ch, 64));
-        const uint4 wk1 = *reinterpret_cast<const uint4 *>(sm + RAW_K + chunk_off(r1, ch, 64));
-        const uint4 wg0 = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(r0, ch, 64));
-        const uint4 wg1 = *reinterpret_cast<const uint4 *>(sm + RAW_G + chunk_off(r1, ch, 64));
-        __syncthreads();   // R1 may now be overwritten
-        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
 
         // (2) cumulative decays and the operand tiles
         {
-            float g0[8], g1[8];
-            unpack_bf16(wg0, g0);
-            unpack_bf16(wg1, g1);
-            const bool v0 = r0 < L, v1 = r1 < L;
+            const int ch = 8 * warp, sw = (lane >> 2) & 1;
+            const int rA = 2 * lane + sw, rB = 2 * lane + 1 - sw;
+            float gA[8], gB[8];
+            unpack_bf16(wgA, gA);
+            unpack_bf16(wgB, gB);
+            const bool vA = rA < L, vB = rB < L;
             // G at rows 2l and 2l+1: inclusive warp scan of the row-pair sums
             float gref[8], glast[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float a = v0 ? g0[i] : 0.f, b = v1 ? g1[i] : 0.f;
+                const float a = vA ? gA[i] : 0.f, b = vB ? gB[i] : 0.f;
                 float s2 = a + b;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float t = __shfl_up_sync(0xffffffffu, s2, off);
                     if (lane >= off) s2 += t;
                 }
-                g0[i] = s2 - b;   // G at row 2l
-                g1[i] = s2;       // G at row 2l + 1
+                const float odd = sw ? a : b;   // the term of row 2l + 1
+                gA[i] = sw ? s2 : s2 - odd;
+                gB[i] = sw ? s2 - odd : s2;
                 gref[i] = __shfl_sync(0xffffffffu, s2, 15);    // G at row 31
                 glast[i] = __shfl_sync(0xffffffffu, s2, 31);   // G at row 63 (= last valid row)
             }
@@ -518,12 +599,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                const int r = half ? r1 : r0;
-                const bool valid = half ? v1 : v0;
-                const float *g = half ? g1 : g0;
+                const int r = half ? rB : rA;
+                const bool valid = half ? vB : vA;
+                const float *g = half ? gB : gA;
                 float qq[8], kk[8];
-                unpack_bf16(half ? wq1 : wq0, qq);
-                unpack_bf16(half ? wk1 : wk0, kk);
+                unpack_bf16(half ? wqB : wqA, qq);
+                unpack_bf16(half ? wkB : wkA, kk);
                 float kf[8], kb[8], kt[8], ke[8], qr[8], qt[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -604,22 +685,32 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         __syncthreads();
 
         // (5) T = (I + A)^-1 in 16 x 16 blocks: diagonal blocks T_II by forward
-        //     substitution (warp I, lane = column), then each warp completes its
-        //     block column (solve_block_column).
-        if (warp < 4 && lane < 16) {
-            const int I = warp, col = lane;
+        //     substitution (warps 0-1, one block per half-warp, lane = column),
+        //     then each warp completes its block column (solve_block_column).
+        //     Meanwhile the warps of TMEM lanes 64..127 write out the previous
+        //     chunk's O, which nothing overwrites before G2.
+        if (warp < 2) {
+            const int I = 2 * warp + (lane >> 4), col = lane & 15;
+            const float *Ab = As + 16 * I * AS + 16 * I;   // diagonal block I, row stride AS
+            // Column-oriented substitution: once x[j] is final, every later row
+            // takes its term.  The chain is one FMA per step; rows load their
+            // four entries of a column group as one 16-byte vector.
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
 #pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                float a0 = 0.f, a1 = 0.f;
+            for (int j0 = 0; j0 < 16; j0 += 4) {
+                float4 a[16];
 #pragma unroll
-                for (int j = 0; j < r; ++j) {
-                    const float a = As[(16 * I + r) * AS + 16 * I + j] * x[j];
-                    if (j & 1) a1 += a; else a0 += a;
+                for (int r = j0 + 1; r < 16; ++r) a[r] = *reinterpret_cast<const float4 *>(Ab + r * AS + j0);
+#pragma unroll
+                for (int j = j0; j < j0 + 4 && j < 15; ++j) {
+#pragma unroll
+                    for (int r = j + 1; r < 16; ++r) {
+                        const float e = (j & 3) == 0 ? a[r].x : (j & 3) == 1 ? a[r].y : (j & 3) == 2 ? a[r].z : a[r].w;
+                        x[r] = fmaf(-e, x[j], x[r]);
+                    }
                 }
-                if (r > col) x[r] = -(a0 + a1);
             }
             const int c = 16 * I + col;
             const float bc = beta_s[c];
@@ -630,7 +721,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OP_TBZ + rr * 128 + ((((c >> 3) ^ rr) & 7) << 4) +
                                                    (c & 7) * 2) = __float2bfloat16_rn(x[r] * bc);
             }
-        } else if (warp >= 4) {
+        } else if (lq >= 2 && c > 0) {
+            store_o_tma(p, sm, sbase, tmem, lq, cq, lane, t0 - C, h);
+            tc_fence_before();
+        }
+        if (warp >= 4) {
             // zero blocks above the diagonal of T Diag(b) and the zero rows 64..127
             const int t = tid - 128;                   // 0 .. 383
             *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * t) = make_uint4(0, 0, 0, 0);
@@ -652,6 +747,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         if (warp < 2) solve_block_column<0>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
         else if (warp < 4) solve_block_column<1>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
         else if (warp < 6) solve_block_column<2>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
+        if (lq >= 2 && lane == 0 && c > 0) tma_store_wait_read();   // the O boxes before the -W read-out
         fence_proxy_async();
         __syncthreads();
 
@@ -731,35 +827,30 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             }
             mma_commit(bar_mma);
         }
+        // the next chunk's raw tiles (prefetched after G1) into registers; the
+        // barrier of the G4 wait then frees them for the next prep.  After the
+        // last chunk the shared-memory reads still run (their values go unused)
+        // so that these registers are never live across a whole chunk.
+        if (c + 1 < nchunks && !mbar_wait(bar_qkg, par ^ 1u)) atomicOr(flags, FLAG_TIMEOUT);
+        load_raw();
         mma_wait_all(bar_mma, 1, flags);
-        // (11) outputs (rows 64..127 of cols 128..255) and the state update
-        if (lq >= 2) {
-            uint32_t r[32];
-            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
-            tmem_wait_ld();
-            const int row = 32 * (lq - 2) + lane;
-            if (row < L) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + row) * p.H + h) * VD + 32 * cq);
-                const float sc = p.scale;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float *f = reinterpret_cast<const float *>(r + 8 * j);
-                    dst[j] = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
-                                        pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
-                }
-            }
-        }
+        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+        // (11) the state update (O is written out during the next chunk's solve)
         {
-            uint32_t r[32];
-            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
-            tmem_wait_ld();
+            // two 16-column reads keep the next chunk's raw tiles in registers
             const float gm = gam_s[(c & 1) * 128 + srow];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = fmaf(gm, S[j], __uint_as_float(r[j]));
-            if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t r[16];
+                KDA_TMEM_LD16(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq + 16 * hh, r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                store_f16(sm, OP_S + chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
+                for (int j = 0; j < 16; ++j) S[16 * hh + j] = fmaf(gm, S[16 * hh + j], __uint_as_float(r[j]));
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    store_f16(sm, OP_S + chunk_off(srow, 32 * cq + 16 * hh + 8 * j, 128), S + 16 * hh + 8 * j);
+            }
+            if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
             // the exact state after (m + 1) * ckpt_chunks full chunks
             const int m = (c + 1) / max(p.ckpt_chunks, 1) - 1;
             if (nck > 0 && (c + 1) % p.ckpt_chunks == 0 && m < nck && !(*flags & FLAG_TIMEOUT)) {
@@ -778,12 +869,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         // before G1 overwrites the columns, and these S stores before G3 reads
         // them (they reach the MMA's proxy through the fence below).  gam_s is
         // double-buffered by chunk parity; nothing else this epilogue reads is
-        // written before that barrier.
+        // written before that barrier.  O stays in columns 128..255 until the
+        // next chunk's G2.
         fence_proxy_async();
         tc_fence_before();
     }
     __syncthreads();
     if (*flags & FLAG_TIMEOUT) aborted = true;
+    if (!aborted && nchunks > 0 && lq >= 2) {
+        tc_fence_after();
+        const int tl = bos + (nchunks - 1) * C;
+        store_o(p, tmem, lq, cq, lane, tl, eos - tl, h);
+    }
 
     if ((*flags & FLAG_RANGE) && tid == 0) report(p.err, DEVERR_RANGE);
     if (aborted) {
@@ -802,6 +899,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 __stcs(d2 + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
         }
     }
+    if (lq >= 2 && lane == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
@@ -831,16 +929,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [T][H][128] bf16 viewed as a 3-D tensor {128, H, T}; boxes of 64 channels x 1 head x 64 tokens.
-bool make_map(CUtensorMap *m, const void *base, int H, int T) {
+// [T][H][128] bf16 viewed as a 3-D tensor {128, H, T}; boxes of bc channels x 1 head x bt tokens.
+bool make_map(CUtensorMap *m, const void *base, int H, int T, cuuint32_t bc = 64, cuuint32_t bt = C,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {bc, 1, bt};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -852,7 +951,8 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
     memset(&p, 0, sizeof(p));
     if (a.T_total > 0) {
         if (!make_map(&p.tq, a.q, a.H, a.T_total) || !make_map(&p.tk, a.k, a.H, a.T_total) ||
-            !make_map(&p.tg, a.gk, a.H, a.T_total) || !make_map(&p.tv, a.v, a.H, a.T_total))
+            !make_map(&p.tg, a.gk, a.H, a.T_total) || !make_map(&p.tv, a.v, a.H, a.T_total) ||
+            !make_map(&p.to, a.o, a.H, a.T_total, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
     p.N = a.N; p.T_total = a.T_total; p.H = a.H; p.num_slots = a.num_slots;
