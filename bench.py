@@ -451,13 +451,15 @@ def bench_prefill_fused(args, ws):
     o = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
     out = torch.empty(T, H, VD, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    record = {"on": False}
+    # per-kernel times: five consecutive steps, each with its own events, queued
+    # behind two unrecorded steps so that no host launch gap falls inside them
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(5)]
+    record = {"ev": None}
     scale = KD ** -0.5
 
     def mark(i):
-        if record["on"]:
-            ev[i].record(stream)
+        if record["ev"] is not None:
+            record["ev"][i].record(stream)
 
     def step():
         mark(0)
@@ -472,13 +474,14 @@ def bench_prefill_fused(args, ws):
 
     K = max(3, min(args.steps, 200))
     ms = timed(step, K, 3, ws)
-    times = []
-    for _ in range(5):
-        record["on"] = True
+    step()
+    step()
+    for evs in ev_sets:
+        record["ev"] = evs
         step()
-        torch.cuda.synchronize()
-        record["on"] = False
-        times.append([ev[i].elapsed_time(ev[i + 1]) for i in range(3)])
+    record["ev"] = None
+    torch.cuda.synchronize()
+    times = [[evs[i].elapsed_time(evs[i + 1]) for i in range(3)] for evs in ev_sets]
     med = [statistics.median(t[i] for t in times) for i in range(3)]
     th = T * H
     pro_bytes = th * (3 * KD * 2 + 2 + 3 * KD * 2 + 2) + 2 * N * H * 3 * 3 * KD * 2

@@ -245,8 +245,13 @@ __global__ void __launch_bounds__(CTA_THREADS, 2)
             if (half == 0) {
                 float y[LANE_CH];
 #pragma unroll
-                for (int e = 0; e < LANE_CH; ++e)
-                    y[e] = gated_norm(ov[e], f, to_f(sm.wn_s[c0 + e]), to_f(sm.gate_s[c0 + e]));
+                for (int e = 0; e < LANE_CH; e += 2) {
+                    const float2 r = gated_norm2(make_float2(ov[e], ov[e + 1]), f,
+                                                 make_float2(to_f(sm.wn_s[c0 + e]), to_f(sm.wn_s[c0 + e + 1])),
+                                                 make_float2(to_f(sm.gate_s[c0 + e]), to_f(sm.gate_s[c0 + e + 1])));
+                    y[e] = r.x;
+                    y[e + 1] = r.y;
+                }
                 store8((T *)a.out + (size_t)u * VD + c0, y);
             }
         }

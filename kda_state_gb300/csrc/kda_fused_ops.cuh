@@ -4,11 +4,15 @@
 // Layout shared by every kernel that computes these steps: a 128-channel row
 // (one token and head) is held by 16 consecutive lanes of a warp, lane j of the
 // half-warp owning channels 8j .. 8j+7, moved as 16-byte vectors (bf16) or
-// pairs of them (fp32).  A row's sum of squares is a sequential FMA chain over
-// the lane's 8 values followed by a butterfly over the 16 lanes, with explicit
-// round-to-nearest intrinsics so nothing can be contracted differently in two
-// kernels.  The fused decode kernel and the unfused prologue / norm kernels go
-// through these same helpers, which is what makes them bit-identical.
+// pairs of them (fp32).  The arithmetic runs on channel pairs (2p, 2p + 1)
+// through the two-wide fp32 instructions (__ffma2_rn, __fmul2_rn, __fadd2_rn):
+// each half rounds exactly as the scalar round-to-nearest instruction would, in
+// half the issue slots.  A row's sum of squares is two FMA chains over the
+// lane's even and odd channels, their sum, and a butterfly over the 16 lanes.
+// Explicit round-to-nearest intrinsics leave nothing to be contracted
+// differently in two kernels: the fused decode kernel and the unfused prologue
+// / norm kernels go through these same helpers, which is what makes them
+// bit-identical.
 #pragma once
 
 #include "kda_common.cuh"
@@ -39,12 +43,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float sigmoid_f(float x) {
     return rcp_approx(__fadd_rn(1.f, ex2_approx(__fmul_rn(x, -1.4426950408889634f))));
 }
-__device__ __forceinline__ float silu_f(float y) { return __fmul_rn(y, sigmoid_f(y)); }
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+// sigmoid_f and SiLU on a channel pair (the same operations per half).
+__device__ __forceinline__ float2 sigmoid2(float2 x) {
+    const float2 e = __fmul2_rn(x, f2(-1.4426950408889634f));
+    const float2 d = __fadd2_rn(f2(1.f), make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+    return make_float2(rcp_approx(d.x), rcp_approx(d.y));
+}
+__device__ __forceinline__ float2 silu2(float2 y) { return __fmul2_rn(y, sigmoid2(y)); }
 
 // The value an unfused path would store and read back.
 template <typename T>
 __device__ __forceinline__ float round_t(float x) {
     return to_f(from_f<T>(x));
+}
+template <typename T> __device__ __forceinline__ float2 round2(float2 x);
+template <> __device__ __forceinline__ float2 round2<float>(float2 x) { return x; }
+template <> __device__ __forceinline__ float2 round2<__nv_bfloat16>(float2 x) {
+    return __bfloat1622float2(__floats2bfloat162_rn(x.x, x.y));
 }
 
 // 8 consecutive elements (16-byte aligned) as float.
@@ -110,15 +126,10 @@ __device__ __forceinline__ float el(const Pack8<float> &v, int e) {
     return e == 0 ? v.a.x : e == 1 ? v.a.y : e == 2 ? v.a.z : e == 3 ? v.a.w
          : e == 4 ? v.b.x : e == 5 ? v.b.y : e == 6 ? v.b.z : v.b.w;
 }
-
-// Causal conv of one channel and SiLU: win[0..W-2] are the previous raw
-// inputs, oldest first; x is the current one; w the channel's W taps.
-__device__ __forceinline__ float conv_silu(const float *w, const float *win, float x) {
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < CONV_TAPS; ++i) acc = __fmaf_rn(w[i], win[i], acc);
-    acc = __fmaf_rn(w[CONV_TAPS], x, acc);
-    return silu_f(acc);
+// Elements 2p and 2p + 1.
+template <typename T>
+__device__ __forceinline__ float2 el2(const Pack8<T> &v, int p) {
+    return make_float2(el(v, 2 * p), el(v, 2 * p + 1));
 }
 
 // Sum of squares of the row held by this lane's half-warp (every lane of the
@@ -126,9 +137,13 @@ __device__ __forceinline__ float conv_silu(const float *w, const float *win, flo
 // half-warp get the same bits: IEEE addition is commutative, so the two lanes
 // of each butterfly pair add the same operands.
 __device__ __forceinline__ float row_sumsq(const float (&x)[LANE_CH]) {
-    float p = __fmul_rn(x[0], x[0]);
+    float2 q = __fmul2_rn(make_float2(x[0], x[1]), make_float2(x[0], x[1]));
 #pragma unroll
-    for (int i = 1; i < LANE_CH; ++i) p = __fmaf_rn(x[i], x[i], p);
+    for (int i = 2; i < LANE_CH; i += 2) {
+        const float2 v = make_float2(x[i], x[i + 1]);
+        q = __ffma2_rn(v, v, q);
+    }
+    float p = __fadd_rn(q.x, q.y);
 #pragma unroll
     for (int off = ROW_LANES / 2; off > 0; off >>= 1)
         p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
@@ -145,9 +160,9 @@ __device__ __forceinline__ float rms_factor(float ss, float eps) {
     return rsqrtf(__fadd_rn(__fmul_rn(ss, 0.0078125f), eps));
 }
 
-// One channel of the gated RMSNorm output.
-__device__ __forceinline__ float gated_norm(float o, float r, float w, float g) {
-    return __fmul_rn(__fmul_rn(__fmul_rn(o, r), w), sigmoid_f(g));
+// Two channels of the gated RMSNorm output: o r w sigmoid(g), left to right.
+__device__ __forceinline__ float2 gated_norm2(float2 o, float r, float2 w, float2 g) {
+    return __fmul2_rn(__fmul2_rn(__fmul2_rn(o, f2(r)), w), sigmoid2(g));
 }
 
 // Conv state element: [slot][tap][stream][H][K].
@@ -158,7 +173,8 @@ __device__ __forceinline__ size_t conv_state_idx(int slot, int tap, int stream, 
 // The W taps of 8 channels c0 .. c0+7 of one stream and head: 8 x W elements,
 // contiguous in conv_w [3][H][K][W] (16-byte aligned); tap i of channel e is
 // element (e W + i) of the run.  Kept packed (load_taps) or unpacked once into
-// floats (unpack_taps) -- the values are the same.
+// float pairs, w[p][i] = taps i of channels 2p and 2p + 1 (unpack_taps) -- the
+// values are the same.
 template <typename T>
 __device__ __forceinline__ void load_taps(const T *conv_w, int stream, int H, int h, int c0,
                                           Pack8<T> (&w)[CONV_W]) {
@@ -167,23 +183,29 @@ __device__ __forceinline__ void load_taps(const T *conv_w, int stream, int H, in
     for (int i = 0; i < CONV_W; ++i) ld8(p + i * LANE_CH, w[i]);
 }
 template <typename T>
-__device__ __forceinline__ void unpack_taps(const Pack8<T> (&p)[CONV_W], float (&w)[LANE_CH][CONV_W]) {
-#pragma unroll
-    for (int e = 0; e < LANE_CH; ++e)
-#pragma unroll
-        for (int i = 0; i < CONV_W; ++i) w[e][i] = el(p[(e * CONV_W + i) / LANE_CH], (e * CONV_W + i) % LANE_CH);
-}
-template <typename T>
 __device__ __forceinline__ float tap(const Pack8<T> (&w)[CONV_W], int e, int i) {
     return el(w[(e * CONV_W + i) / LANE_CH], (e * CONV_W + i) % LANE_CH);
 }
-__device__ __forceinline__ float tap(const float (&w)[LANE_CH][CONV_W], int e, int i) { return w[e][i]; }
-
-// Conv windows (the W-1 previous raw inputs of 8 channels): packed rows or
-// floats, with the same values.
 template <typename T>
-__device__ __forceinline__ float wget(const Pack8<T> (&win)[CONV_TAPS], int i, int e) { return el(win[i], e); }
-__device__ __forceinline__ float wget(const float (&win)[CONV_TAPS][LANE_CH], int i, int e) { return win[i][e]; }
+__device__ __forceinline__ void unpack_taps(const Pack8<T> (&p)[CONV_W], float2 (&w)[LANE_CH / 2][CONV_W]) {
+#pragma unroll
+    for (int q = 0; q < LANE_CH / 2; ++q)
+#pragma unroll
+        for (int i = 0; i < CONV_W; ++i) w[q][i] = make_float2(tap(p, 2 * q, i), tap(p, 2 * q + 1, i));
+}
+template <typename T>
+__device__ __forceinline__ float2 tap2(const Pack8<T> (&w)[CONV_W], int p, int i) {
+    return make_float2(tap(w, 2 * p, i), tap(w, 2 * p + 1, i));
+}
+__device__ __forceinline__ float2 tap2(const float2 (&w)[LANE_CH / 2][CONV_W], int p, int i) { return w[p][i]; }
+
+// Conv windows (the W-1 previous raw inputs of 8 channels, oldest first): packed
+// rows or float pairs, with the same values.
+template <typename T>
+__device__ __forceinline__ float2 wget2(const Pack8<T> (&win)[CONV_TAPS], int i, int p) { return el2(win[i], p); }
+__device__ __forceinline__ float2 wget2(const float2 (&win)[CONV_TAPS][LANE_CH / 2], int i, int p) {
+    return win[i][p];
+}
 template <typename T>
 __device__ __forceinline__ void wshift(Pack8<T> (&win)[CONV_TAPS], const Pack8<T> &x) {
 #pragma unroll
@@ -191,27 +213,30 @@ __device__ __forceinline__ void wshift(Pack8<T> (&win)[CONV_TAPS], const Pack8<T
     win[CONV_TAPS - 1] = x;
 }
 template <typename T>
-__device__ __forceinline__ void wshift(float (&win)[CONV_TAPS][LANE_CH], const Pack8<T> &x) {
+__device__ __forceinline__ void wshift(float2 (&win)[CONV_TAPS][LANE_CH / 2], const Pack8<T> &x) {
 #pragma unroll
-    for (int e = 0; e < LANE_CH; ++e) {
+    for (int p = 0; p < LANE_CH / 2; ++p) {
 #pragma unroll
-        for (int i = 0; i + 1 < CONV_TAPS; ++i) win[i][e] = win[i + 1][e];
-        win[CONV_TAPS - 1][e] = el(x, e);
+        for (int i = 0; i + 1 < CONV_TAPS; ++i) win[i][p] = win[i + 1][p];
+        win[CONV_TAPS - 1][p] = el2(x, p);
     }
 }
 
-// Conv + SiLU of one token on 8 channels; shifts x into the window.  y gets
-// the outputs rounded to T (the stored conv output).
+// Causal conv + SiLU of one token on 8 channels: per channel the taps times
+// the window (oldest first) then the current input, accumulated by FMA from 0;
+// shifts x into the window.  y gets the outputs rounded to T (the stored conv
+// output).
 template <typename T, typename Taps, typename Win>
 __device__ __forceinline__ void conv8(const Taps &w, Win &win, const Pack8<T> &x, float (&y)[LANE_CH]) {
 #pragma unroll
-    for (int e = 0; e < LANE_CH; ++e) {
-        float wt[CONV_W], wv[CONV_TAPS];
+    for (int p = 0; p < LANE_CH / 2; ++p) {
+        float2 acc = f2(0.f);
 #pragma unroll
-        for (int i = 0; i < CONV_W; ++i) wt[i] = tap(w, e, i);
-#pragma unroll
-        for (int i = 0; i < CONV_TAPS; ++i) wv[i] = wget(win, i, e);
-        y[e] = round_t<T>(conv_silu(wt, wv, el(x, e)));
+        for (int i = 0; i < CONV_TAPS; ++i) acc = __ffma2_rn(tap2(w, p, i), wget2(win, i, p), acc);
+        acc = __ffma2_rn(tap2(w, p, CONV_TAPS), el2(x, p), acc);
+        const float2 r = round2<T>(silu2(acc));
+        y[2 * p] = r.x;
+        y[2 * p + 1] = r.y;
     }
     wshift(win, x);
 }
@@ -221,7 +246,11 @@ template <typename T>
 __device__ __forceinline__ void l2norm8(float (&y)[LANE_CH], float eps) {
     const float f = l2_factor(row_sumsq(y), eps);
 #pragma unroll
-    for (int e = 0; e < LANE_CH; ++e) y[e] = __fmul_rn(y[e], f);
+    for (int p = 0; p < LANE_CH / 2; ++p) {
+        const float2 v = __fmul2_rn(make_float2(y[2 * p], y[2 * p + 1]), f2(f));
+        y[2 * p] = v.x;
+        y[2 * p + 1] = v.y;
+    }
 }
 
 }  // namespace kda

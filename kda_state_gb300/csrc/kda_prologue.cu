@@ -3,7 +3,9 @@
 // and k, beta = sigmoid(b) (one kernel), and the gated RMSNorm of the output
 // read at its own strides (another).  Both move 16-byte vectors, 8 channels
 // per lane, and reduce each 128-channel row over a half-warp with the helpers
-// of kda_fused_ops.cuh.
+// of kda_fused_ops.cuh.  The prologue streams its raw inputs through a
+// per-warp ring of asynchronous copies (cp.async) so that each warp keeps
+// PRO_DEPTH - 1 tokens in flight while it computes.
 //
 // Paper correspondence: Kimi K3 on B200 deployment notes, items "prefill /
 // decode kernel fusion" and "other prefill switches": the three conv1d, the
@@ -19,7 +21,29 @@ namespace {
 constexpr int PRO_TILE = 64;                  // tokens per CTA
 constexpr int PRO_HEADS = 2;                  // heads per CTA
 constexpr int PRO_THREADS = 3 * 32;           // warp w: stream w, heads lane / 16
-constexpr int PRO_PREFETCH = 4;               // tokens loaded ahead of the conv
+constexpr int PRO_DEPTH = 16;                 // ring slots per warp
+constexpr int PRO_TOK = 4;                    // tokens per iteration (independent chains)
+
+// 16-byte asynchronous copy global -> shared (zero-filled when !ok: no global
+// read), one commit group per call site, and the wait for all but the newest
+// N groups of this thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void cp_async_pack(Pack8<T> *dst, const T *src, bool ok) {
+    static_assert(sizeof(Pack8<T>) % 16 == 0, "16-byte pieces");
+#pragma unroll
+    for (int i = 0; i < (int)sizeof(Pack8<T>) / 16; ++i)
+        cp_async16(reinterpret_cast<uint8_t *>(dst) + 16 * i, reinterpret_cast<const uint8_t *>(src) + 16 * i, ok);
+}
 
 // grid: (N x max_tiles, ceil(H / 2)).  The CTA of tile 0 also reads the
 // sequence's conv state and writes the new one, so an in-place slot has one
@@ -51,8 +75,8 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
     const size_t col = (size_t)(live ? h : 0) * KD + c0;
     const size_t hk = (size_t)a.H * KD;
 
-    // taps and windows unpacked once: every token reuses them
-    float w[LANE_CH][CONV_W], win[CONV_TAPS][LANE_CH];
+    // taps and windows unpacked once into channel pairs: every token reuses them
+    float2 w[LANE_CH / 2][CONV_W], win[CONV_TAPS][LANE_CH / 2];
     {
         Pack8<T> wp[CONV_W], wn[CONV_TAPS];
 #pragma unroll
@@ -75,27 +99,54 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
 #pragma unroll
         for (int i = 0; i < CONV_TAPS; ++i)
 #pragma unroll
-            for (int e = 0; e < LANE_CH; ++e) win[i][e] = el(wn[i], e);
+            for (int q = 0; q < LANE_CH / 2; ++q) win[i][q] = el2(wn[i], q);
     }
-    for (int j0 = 0; j0 < cnt; j0 += PRO_PREFETCH) {
-        Pack8<T> x[PRO_PREFETCH];
+    // Ring of PRO_DEPTH token slots per warp; lane l owns bytes [l, l + 1) x
+    // sizeof(Pack8<T>) of every slot and reads back only what it copied, so no
+    // lane waits for another.  Tokens go PRO_TOK per iteration (independent
+    // chains after the conv); the iteration at token j copies tokens
+    // j + PRO_DEPTH - PRO_TOK .. j + PRO_DEPTH - 1 into the slots of tokens
+    // j - PRO_TOK .. j - 1, read and consumed by the previous iteration.  A
+    // token past the tile is zero-filled, computed and not stored.
+    static_assert((PRO_DEPTH & (PRO_DEPTH - 1)) == 0 && PRO_DEPTH > PRO_TOK, "ring");
+    __shared__ __align__(16) Pack8<T> ring[PRO_THREADS / 32][PRO_DEPTH][32];
+    Pack8<T> (&my)[PRO_DEPTH][32] = ring[warp];
+    const T *gsrc = raw + (size_t)t0 * a.raw_stride + col;   // row t0: valid whenever cnt > 0
+    const T *gnext = gsrc;
+    int jn = 0;   // next token to copy
+    auto issue = [&]() {
+        const bool ok = live && jn < cnt;
+        cp_async_pack<T>(&my[jn & (PRO_DEPTH - 1)][lane], ok ? gnext : gsrc, ok);
+        cp_async_commit();
+        gnext += a.raw_stride;
+        ++jn;
+    };
+#pragma unroll 1
+    for (int j = 0; j < PRO_DEPTH - PRO_TOK && cnt > 0; ++j) issue();   // none for an empty sequence
+    T *dptr = dst + (size_t)t0 * hk + col;
+#pragma unroll 1
+    for (int j = 0; j < cnt; j += PRO_TOK) {   // cnt is uniform across the CTA
 #pragma unroll
-        for (int p = 0; p < PRO_PREFETCH; ++p) {
-            if (live && j0 + p < cnt)
-                ld8(raw + (size_t)(t0 + j0 + p) * a.raw_stride + col, x[p]);
-            else
-                zero8(x[p]);
-        }
+        for (int u = 0; u < PRO_TOK; ++u) issue();
+        cp_async_wait<PRO_DEPTH - PRO_TOK>();   // tokens j .. j + PRO_TOK - 1 have landed
+        Pack8<T> x[PRO_TOK];
 #pragma unroll
-        for (int p = 0; p < PRO_PREFETCH; ++p) {
-            if (j0 + p < cnt) {   // uniform across the CTA
-                float y[LANE_CH];
-                conv8<T>(w, win, x[p], y);
-                if (s < 2) l2norm8<T>(y, a.eps);
-                if (live) store8(dst + (size_t)(t0 + j0 + p) * hk + col, y);
-            }
+        for (int u = 0; u < PRO_TOK; ++u) x[u] = my[(j + u) & (PRO_DEPTH - 1)][lane];
+        float y[PRO_TOK][LANE_CH];
+#pragma unroll
+        for (int u = 0; u < PRO_TOK; ++u) conv8<T>(w, win, x[u], y[u]);
+        if (s < 2) {
+#pragma unroll
+            for (int u = 0; u < PRO_TOK; ++u) l2norm8<T>(y[u], a.eps);
         }
+        if (live) {
+#pragma unroll
+            for (int u = 0; u < PRO_TOK; ++u)
+                if (j + u < cnt) store8(dptr + u * hk, y[u]);
+        }
+        dptr += PRO_TOK * hk;
     }
+    cp_async_wait<0>();
     if (s == 2 && live) {
         for (int i = lane & 15; i < cnt; i += ROW_LANES) {
             const size_t bi = (size_t)(t0 + i) * a.H + h;
@@ -146,7 +197,12 @@ __global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormAr
         const float f = rms_factor(row_sumsq(o), a.eps);
         float y[LANE_CH];
 #pragma unroll
-        for (int e = 0; e < LANE_CH; ++e) y[e] = gated_norm(o[e], f, wn[e], g[e]);
+        for (int e = 0; e < LANE_CH; e += 2) {
+            const float2 r = gated_norm2(make_float2(o[e], o[e + 1]), f, make_float2(wn[e], wn[e + 1]),
+                                         make_float2(g[e], g[e + 1]));
+            y[e] = r.x;
+            y[e + 1] = r.y;
+        }
         if (live) store8((T *)a.out + (size_t)row * VD + c0, y);
     }
 }
