@@ -81,6 +81,12 @@ constexpr uint32_t OP_S = 163840;      // S0, fp16, 128 rows (k) x 128 (v), MN-m
 constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 128 ch, MN-major A
 constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
 constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
+// Before the first chunk and after the last, the fp32 state passes through a
+// 64 KB staging tile here (KT, [-W; Q~] and the first half of S0), rows of 512
+// bytes with the 16-byte chunks of each row XOR-swizzled by (row & 7): whole
+// rows move to and from HBM coalesced, and each thread's 128-byte row segment
+// is read or written without bank conflicts.
+constexpr uint32_t STG = OP_KT;
 constexpr uint32_t SM_BETA = 229376;   // fp32 [64]
 constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [2][128]: exp(G_L), by chunk parity
 constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 3 mbarriers
@@ -471,6 +477,19 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         mbar_init(bar_mma, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *flags = 0;
+        // the first chunk's raw tiles, issued before anything else so that they
+        // land while TMEM is allocated and the state is loaded
+        if (nchunks > 0) {
+            mbar_expect_tx(bar_qkg, 3 * 16384);
+            for (int b = 0; b < 2; ++b) {
+                tma_load_3d(sbase + RAW_Q + b * 8192, &p.tq, bar_qkg, 64 * b, h, bos);
+                tma_load_3d(sbase + RAW_K + b * 8192, &p.tk, bar_qkg, 64 * b, h, bos);
+                tma_load_3d(sbase + RAW_G + b * 8192, &p.tg, bar_qkg, 64 * b, h, bos);
+            }
+            mbar_expect_tx(bar_v, 16384);
+            for (int b = 0; b < 2; ++b)
+                tma_load_3d(sbase + RAW_V + b * 8192, &p.tv, bar_v, 64 * b, h, bos);
+        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -483,33 +502,34 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (tid == 0 && nchunks > 0) {
-        mbar_expect_tx(bar_qkg, 3 * 16384);
-        for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sbase + RAW_Q + b * 8192, &p.tq, bar_qkg, 64 * b, h, bos);
-            tma_load_3d(sbase + RAW_K + b * 8192, &p.tk, bar_qkg, 64 * b, h, bos);
-            tma_load_3d(sbase + RAW_G + b * 8192, &p.tg, bar_qkg, 64 * b, h, bos);
-        }
-        mbar_expect_tx(bar_v, 16384);
-        for (int b = 0; b < 2; ++b)
-            tma_load_3d(sbase + RAW_V + b * 8192, &p.tv, bar_v, 64 * b, h, bos);
-    }
 
     // ---- initial state: row k = 32*lq + lane, columns 32*cq .. 32*cq+31 ---
     const int srow = 32 * lq + lane;
+    float *stg = reinterpret_cast<float *>(sm + STG);
     float S[32];
-    if (si >= 0) {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            p.pool + ((size_t)si * p.H + h) * STATE_ELEMS + (size_t)srow * VD + 32 * cq);
+    if (si >= 0) {   // uniform across the CTA
+        const float4 *src = reinterpret_cast<const float4 *>(p.pool + ((size_t)si * p.H + h) * STATE_ELEMS);
+        // all eight loads are issued before the first store: a store through the
+        // generic staging pointer may not be moved above a later global load
+        float4 t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = __ldcs(src + i * NT + tid);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {   // float4 e of the state: row e / 32, chunk e % 32
+            const int e = i * NT + tid, r = e >> 5, c4 = e & 31;
+            *reinterpret_cast<float4 *>(stg + r * VD + 4 * (c4 ^ (r & 7))) = t[i];
+        }
+        __syncthreads();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 t = __ldcs(src + j);
+            const float4 t = *reinterpret_cast<const float4 *>(stg + srow * VD + 4 * ((8 * cq + j) ^ (srow & 7)));
             S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[j] = 0.f;
     }
+    __syncthreads();   // the staging tile is read before the S0 tile over it is written
     if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
 #pragma unroll
     for (int j = 0; j < 4; ++j) store_f16(sm + OP_S, chunk_off(srow, 32 * cq + 8 * j, 128), S + 8 * j);
@@ -885,18 +905,24 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     if ((*flags & FLAG_RANGE) && tid == 0) report(p.err, DEVERR_RANGE);
     if (aborted) {
         if (tid == 0) report(p.err, DEVERR_TIMEOUT);
-    } else {
-        float4 *dst = reinterpret_cast<float4 *>(p.pool + ((size_t)so * p.H + h) * STATE_ELEMS +
-                                                 (size_t)srow * VD + 32 * cq);
+    } else {   // aborted is uniform; no copy or MMA is in flight, all of shared memory is free
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            __stcs(dst + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
-        if (ss >= 0) {
-            float4 *d2 = reinterpret_cast<float4 *>(p.pool + ((size_t)ss * p.H + h) * STATE_ELEMS +
-                                                    (size_t)srow * VD + 32 * cq);
+            *reinterpret_cast<float4 *>(stg + srow * VD + 4 * ((8 * cq + j) ^ (srow & 7))) =
+                make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        __syncthreads();
+        float4 *dst = reinterpret_cast<float4 *>(p.pool + ((size_t)so * p.H + h) * STATE_ELEMS);
+        float4 *d2 = ss >= 0 ? reinterpret_cast<float4 *>(p.pool + ((size_t)ss * p.H + h) * STATE_ELEMS) : nullptr;
+        float4 t[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                __stcs(d2 + j, make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
+        for (int i = 0; i < 8; ++i) {
+            const int e = i * NT + tid, r = e >> 5, c4 = e & 31;
+            t[i] = *reinterpret_cast<const float4 *>(stg + r * VD + 4 * (c4 ^ (r & 7)));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            __stcs(dst + i * NT + tid, t[i]);
+            if (d2) __stcs(d2 + i * NT + tid, t[i]);
         }
     }
     if (lq >= 2 && lane == 0) tma_store_wait_all();
