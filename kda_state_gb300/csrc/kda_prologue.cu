@@ -173,7 +173,11 @@ __global__ void __launch_bounds__(PRO_THREADS) conv_prologue_kernel(const Prolog
     }
 }
 
-// Grid-stride over pairs of (token, head) rows: one row per half-warp.
+// Grid-stride over groups of NORM_PAIRS pairs of (token, head) rows, one row
+// per half-warp: all loads of a group are issued before any row is computed,
+// so each warp keeps NORM_PAIRS x 1 KB in flight.
+constexpr int NORM_PAIRS = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormArgs a) {
     const int lane = threadIdx.x & 31, c0 = (lane & 15) * LANE_CH;
@@ -181,29 +185,39 @@ __global__ void __launch_bounds__(CTA_THREADS) gated_rmsnorm_kernel(const NormAr
     float wn[LANE_CH];
     load8((const T *)a.w_norm + c0, wn);
     const unsigned nwarps = gridDim.x * (CTA_THREADS / 32);
-    for (unsigned pair = blockIdx.x * (CTA_THREADS / 32) + (threadIdx.x >> 5); pair * 2 < rows;
-         pair += nwarps) {
-        const unsigned row = pair * 2 + (lane >> 4);
-        const bool live = row < rows;
-        float o[LANE_CH], g[LANE_CH];
-        if (live) {
-            const unsigned t = row / (unsigned)a.H, h = row - t * (unsigned)a.H;
-            load8((const T *)a.o + (size_t)t * a.o_token_stride + (size_t)h * a.o_head_stride + c0, o);
-            load8((const T *)a.gate + (size_t)row * VD + c0, g);
-        } else {
+    for (unsigned grp = blockIdx.x * (CTA_THREADS / 32) + (threadIdx.x >> 5); grp * 2 * NORM_PAIRS < rows;
+         grp += nwarps) {
+        Pack8<T> ov[NORM_PAIRS], gv[NORM_PAIRS];
+        bool live[NORM_PAIRS];
 #pragma unroll
-            for (int e = 0; e < LANE_CH; ++e) o[e] = g[e] = 0.f;
+        for (int j = 0; j < NORM_PAIRS; ++j) {
+            const unsigned row = (grp * NORM_PAIRS + j) * 2 + (lane >> 4);
+            live[j] = row < rows;
+            if (live[j]) {
+                const unsigned t = row / (unsigned)a.H, h = row - t * (unsigned)a.H;
+                ld8((const T *)a.o + (size_t)t * a.o_token_stride + (size_t)h * a.o_head_stride + c0, ov[j]);
+                ld8((const T *)a.gate + (size_t)row * VD + c0, gv[j]);
+            } else {
+                zero8(ov[j]);
+                zero8(gv[j]);
+            }
         }
-        const float f = rms_factor(row_sumsq(o), a.eps);
-        float y[LANE_CH];
 #pragma unroll
-        for (int e = 0; e < LANE_CH; e += 2) {
-            const float2 r = gated_norm2(make_float2(o[e], o[e + 1]), f, make_float2(wn[e], wn[e + 1]),
-                                         make_float2(g[e], g[e + 1]));
-            y[e] = r.x;
-            y[e + 1] = r.y;
+        for (int j = 0; j < NORM_PAIRS; ++j) {
+            float o[LANE_CH];
+#pragma unroll
+            for (int e = 0; e < LANE_CH; ++e) o[e] = el(ov[j], e);
+            const float f = rms_factor(row_sumsq(o), a.eps);
+            float y[LANE_CH];
+#pragma unroll
+            for (int e = 0; e < LANE_CH; e += 2) {
+                const float2 r = gated_norm2(make_float2(o[e], o[e + 1]), f, make_float2(wn[e], wn[e + 1]),
+                                             el2(gv[j], e / 2));
+                y[e] = r.x;
+                y[e + 1] = r.y;
+            }
+            if (live[j]) store8((T *)a.out + (size_t)((grp * NORM_PAIRS + j) * 2 + (lane >> 4)) * VD + c0, y);
         }
-        if (live) store8((T *)a.out + (size_t)row * VD + c0, y);
     }
 }
 
@@ -224,8 +238,8 @@ cudaError_t launch_gated_rmsnorm(const NormArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t want = (rows + 15) / 16;   // warps of 2 rows, 8 warps per CTA
-    const size_t cap = (size_t)(sms > 0 ? sms : 152) * 8;
+    const size_t want = (rows + 16 * NORM_PAIRS - 1) / (16 * NORM_PAIRS);   // 8 warps of 2 x NORM_PAIRS rows
+    const size_t cap = (size_t)(sms > 0 ? sms : 152) * 16;
     const unsigned grid = (unsigned)(want < cap ? want : cap);
     if (a.dt == KDA_DTYPE_BF16)
         gated_rmsnorm_kernel<__nv_bfloat16><<<grid, CTA_THREADS, 0, s>>>(a);
