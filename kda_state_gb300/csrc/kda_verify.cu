@@ -322,10 +322,10 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                 ((T *)a.rk)[e * KD + c] = kr[i];
                 a.rdecay[e * KD + c] = alpha;
                 E *= alpha;
-                tiny |= !(E > 1e-30f);
+                tiny |= !(E > 1e-30f && E < 1e30f);   // outside: the recurrent fallback
                 const float kk = to_f(kr[i]), qq = to_f(qr[i]);
                 sm.kg[i][c] = kk * E;
-                sm.kn[i][c] = kk / E;
+                sm.kn[i][c] = __fdividef(kk, E);   // used only for E in (1e-30, 1e30): within 2 ulp
                 sm.qg[i][c] = qq * E;
             }
         }
