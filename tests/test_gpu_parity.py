@@ -306,16 +306,20 @@ def test_device_errors_are_reported_and_skipped():
     assert int(err.item()) & kda().KDA_DEVERR_SEQLENS
 
 
-@pytest.mark.parametrize("case", ["strong_decay_fallback", "long_draft_recurrent"])
+@pytest.mark.parametrize("case", ["strong_decay_fallback", "growth_fallback", "long_draft_recurrent"])
 def test_verify_other_paths(case):
     """Verify's other code paths: a draft whose cumulative decay leaves the
-    range of the block form (gk = -12 per step), and G = 20 > 16 drafts."""
+    range of the block form below (gk = -12 per step) or above (gk = +9 per
+    step: the product passes 1e30 at the eighth draft, the state stays far
+    inside fp32), and G = 20 > 16 drafts."""
     g = gen.make_gen(61)
     B, H, S = 3, 2, 6
-    G, R = (8, 16) if case == "strong_decay_fallback" else (20, 64)
+    G, R = (20, 64) if case == "long_draft_recurrent" else (8, 16)
     x = gen.token_inputs(G, H, torch.bfloat16, g, lead=(B,))
     if case == "strong_decay_fallback":
         x["gk"] = torch.full_like(x["gk"], -12.0)
+    if case == "growth_fallback":
+        x["gk"] = torch.full_like(x["gk"], 9.0)
     pool = gen.checkpoint((S, H, KD, VD), g).to(DEV)
     committed = pool.clone()
     ids = torch.tensor([4, 0, 2], dtype=torch.int32, device=DEV)
