@@ -41,6 +41,11 @@
 // triangular inverse (16x16 blocks), the TMEM read-outs and the fp32 state
 // update.  All waits are bounded; a wait that gives up reports
 // KDA_DEVERR_TIMEOUT, frees TMEM and abandons the unit.
+// Data movement around the phases: raw q, k, gk, v tiles arrive by TMA one
+// chunk ahead and are taken into registers while the previous chunk's G4 runs;
+// a chunk's O stays in TMEM until the next chunk's solve phase, where the warps
+// of lanes 64..127 write it with 32 x 32 tensor stores; the unit's initial and
+// final states move as whole 512-byte rows through a swizzled staging tile.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
