@@ -126,9 +126,16 @@ def barrier(ws):
 def max_over_ranks(x, ws):
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units, ms, ws):
+    """Whole-job rate: every rank runs the same replica workload of `units`
+    units, and ms is the slowest rank's time per step."""
+    return units / (ms / 1e3) * ws
 
 
 def timed(fn, steps, warmup, ws, sampler=None, stream=None):
@@ -812,7 +819,7 @@ def main():
         sampler.stop()
     hbm, _, peak_kind = peaks()
     ms = res["ms"]
-    value = res["T"] / (ms / 1e3) * ws
+    value = aggregate_rate(res["T"], ms, ws)
     achieved = res["alg_bytes"] / (ms / 1e3) / 1e9
     traffic = profile_traffic("kda_prefill_tc.cu", "prefill_tc_kernel.varlen.md")
     line = {
@@ -828,7 +835,7 @@ def main():
                      "frac": achieved / hbm, "traffic": traffic,
                      "peak_kind": peak_kind, "kernel": "kda_chunk_prefill",
                      "algorithmic_bytes_per_launch": res["alg_bytes"]},
-        "e2e": {"value": res["T"] / (res["ms_e2e"] / 1e3) * ws, "unit": "tok/s",
+        "e2e": {"value": aggregate_rate(res["T"], res["ms_e2e"], ws), "unit": "tok/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": res["ms_e2e"],
                 "schedule": "pinned host inputs in and o out every step; steps pipelined: the "
@@ -843,7 +850,7 @@ def main():
         try:
             c = bench_varlen_checkpoints(args, ws)
             also["varlen_checkpoints"] = {
-                "tok_per_s": c["T"] / (c["ms"] / 1e3) * ws, "ms_per_step": c["ms"],
+                "tok_per_s": aggregate_rate(c["T"], c["ms"], ws), "ms_per_step": c["ms"],
                 "workload": "the varlen batch above with the state written every %d tokens "
                             "(%d checkpoints per head) into a slot list"
                             % (c["interval"], c["checkpoints"]),
@@ -857,7 +864,7 @@ def main():
         try:
             lg = bench_long(args, ws)
             also["long_prefill"] = {
-                "tok_per_s": lg["tokens"] / (lg["ms"] / 1e3) * ws, "ms_per_step": lg["ms"],
+                "tok_per_s": aggregate_rate(lg["tokens"], lg["ms"], ws), "ms_per_step": lg["ms"],
                 "workload": "4 seqs x 24576 tok, H=96, bf16, from checkpoints, 6 pieces of 4096 "
                             "resuming in place, ping-pong snapshot per piece",
                 "GBps": lg["alg_bytes"] / (lg["ms"] / 1e3) / 1e9,
@@ -869,7 +876,7 @@ def main():
         try:
             d = bench_decode(args, ws)
             also["decode"] = {
-                "tok_per_s": d["B"] / (d["ms"] / 1e3) * ws, "ms_per_step": d["ms"],
+                "tok_per_s": aggregate_rate(d["B"], d["ms"], ws), "ms_per_step": d["ms"],
                 "workload": "384 req x 1 tok, H=64, 512-slot pools, 69 layers, %d CoW copies/layer"
                             % d["n_cow"],
                 "decode_kernel_us": d["dec_ms"] * 1e3,
@@ -883,8 +890,8 @@ def main():
         try:
             v = bench_verify_fold(args, ws)
             also["verify_fold"] = {
-                "accepted_tok_per_s": v["accepted"] / (v["ms"] / 1e3) * ws,
-                "verified_tok_per_s": v["B"] * v["G"] / (v["ms"] / 1e3) * ws,
+                "accepted_tok_per_s": aggregate_rate(v["accepted"], v["ms"], ws),
+                "verified_tok_per_s": aggregate_rate(v["B"] * v["G"], v["ms"], ws),
                 "ms_per_step": v["ms"], "mean_accept": v["mean_accept"],
                 "workload": "64 req x 8 draft tok, 69 layers, H=64, 128-slot pools, ring 16",
                 "verify_kernel_us": v["ver_ms"] * 1e3,
@@ -901,7 +908,7 @@ def main():
         try:
             df = bench_decode_fused(args, ws)
             also["decode_fused"] = {
-                "tok_per_s": df["B"] / (df["ms"] / 1e3) * ws, "ms_per_step": df["ms"],
+                "tok_per_s": aggregate_rate(df["B"], df["ms"], ws), "ms_per_step": df["ms"],
                 "unfused_ms_per_step": df["ms_unfused"],
                 "workload": "384 req x 1 tok, H=64, 512-slot pools, 69 layers: conv + KDA + onorm "
                             "in one launch per layer (unfused: prologue + decode + norm)",
@@ -916,7 +923,7 @@ def main():
         try:
             pf = bench_prefill_fused(args, ws)
             also["prefill_fused_path"] = {
-                "tok_per_s": pf["T"] / (pf["ms"] / 1e3) * ws, "ms_per_step": pf["ms"],
+                "tok_per_s": aggregate_rate(pf["T"], pf["ms"], ws), "ms_per_step": pf["ms"],
                 "workload": "the varlen batch from raw projections: conv prologue, chunked "
                             "prefill, gated RMSNorm",
                 "prologue_us": pf["prologue_ms"] * 1e3,
@@ -944,8 +951,8 @@ def main():
         try:
             v = bench_verify_fold(args, ws, ragged=True)
             also["verify_fold_ragged"] = {
-                "accepted_tok_per_s": v["accepted"] / (v["ms"] / 1e3) * ws,
-                "verified_tok_per_s": v["verified"] / (v["ms"] / 1e3) * ws,
+                "accepted_tok_per_s": aggregate_rate(v["accepted"], v["ms"], ws),
+                "verified_tok_per_s": aggregate_rate(v["verified"], v["ms"], ws),
                 "ms_per_step": v["ms"], "mean_accept": v["mean_accept"],
                 "mean_draft": v["mean_draft"],
                 "workload": "64 req x G_b ~ U{1..8} draft tok (trimmed windows), 69 layers, H=64, "
