@@ -87,14 +87,15 @@ constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 12
 constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
 constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
 // Before the first chunk and after the last, the fp32 state passes through a
-// 64 KB staging tile here (KT, [-W; Q~] and the first half of S0), rows of 512
-// bytes with the 16-byte chunks of each row XOR-swizzled by (row & 7): whole
-// rows move to and from HBM coalesced, and each thread's 128-byte row segment
-// is read or written without bank conflicts.
+// 64 KB staging tile here (KT, [-W; Q~] and the first half of S0).  In: four
+// tensor copies, box j = columns 32j .. 32j+31 of the 128 rows, 128 bytes per
+// row with its 16-byte chunks XOR-swizzled by (row & 7).  Out: rows of 512
+// bytes, chunks XOR-swizzled by (row & 7), stored as whole rows.  Either way
+// each thread's 128-byte row segment moves without bank conflicts.
 constexpr uint32_t STG = OP_KT;
 constexpr uint32_t SM_BETA = 229376;   // fp32 [64]
 constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [2][128]: exp(G_L), by chunk parity
-constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 3 mbarriers
+constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 4 mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
@@ -112,6 +113,7 @@ enum { FLAG_TIMEOUT = 1, FLAG_RANGE = 2 };
 struct Params {
     CUtensorMap tq, tk, tg, tv;
     CUtensorMap to;   // o: boxes of 32 channels x 1 head x 32 tokens, 64-byte swizzle
+    CUtensorMap tpool;   // the state pool as [slots * H * 128][128] fp32: boxes of 32 columns x 128 rows
     int N, T_total, H, num_slots, lpt;
     const __nv_bfloat16 *beta;
     const int32_t *cu;
@@ -170,6 +172,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
 // Bulk tensor store of a shared-memory box; completes in this thread's bulk group.
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *Rws = reinterpret_cast<float *>(sm + SCR_RW);   // per-warp R scratch of the solve
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
-                   bar_mma = sbase + SM_BAR + 16;
+                   bar_mma = sbase + SM_BAR + 16, bar_st = sbase + SM_BAR + 24;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM_MISC);
     int *flags = reinterpret_cast<int *>(sm + SM_MISC + 4);
 
@@ -480,8 +489,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         mbar_init(bar_qkg, 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_st, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *flags = 0;
+        // the initial state, by four tensor copies into the staging tile
+        if (si >= 0) {
+            mbar_expect_tx(bar_st, STATE_ELEMS * sizeof(float));
+            for (int j = 0; j < 4; ++j) tma_load_2d(sbase + STG + j * 16384, &p.tpool, bar_st, 32 * j, (si * p.H + h) * KD);
+        }
         // the first chunk's raw tiles, issued before anything else so that they
         // land while TMEM is allocated and the state is loaded
         if (nchunks > 0) {
@@ -513,21 +528,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *stg = reinterpret_cast<float *>(sm + STG);
     float S[32];
     if (si >= 0) {   // uniform across the CTA
-        const float4 *src = reinterpret_cast<const float4 *>(p.pool + ((size_t)si * p.H + h) * STATE_ELEMS);
-        // all eight loads are issued before the first store: a store through the
-        // generic staging pointer may not be moved above a later global load
-        float4 t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = __ldcs(src + i * NT + tid);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {   // float4 e of the state: row e / 32, chunk e % 32
-            const int e = i * NT + tid, r = e >> 5, c4 = e & 31;
-            *reinterpret_cast<float4 *>(stg + r * VD + 4 * (c4 ^ (r & 7))) = t[i];
-        }
+        if (tid == 0 && !mbar_wait(bar_st, 0)) atomicOr(flags, FLAG_TIMEOUT);
         __syncthreads();
+        const float *box = stg + cq * (KD * 32);   // columns 32 cq .. 32 cq + 31
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 t = *reinterpret_cast<const float4 *>(stg + srow * VD + 4 * ((8 * cq + j) ^ (srow & 7)));
+            const float4 t = *reinterpret_cast<const float4 *>(box + srow * 32 + ((j ^ (srow & 7)) << 2));
             S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
         }
     } else {
@@ -974,6 +980,22 @@ bool make_map(CUtensorMap *m, const void *base, int H, int T, cuuint32_t bc = 64
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The state pool as a 2-D fp32 tensor [num_slots * H * 128 rows][128 columns],
+// boxes of 32 columns x 128 rows (a head's state is four boxes), 128-byte swizzle.
+bool make_pool_map(CUtensorMap *m, const float *pool, int num_slots, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t rows = (cuuint64_t)num_slots * (cuuint64_t)H * KD;
+    if (rows == 0 || rows > 0x7fffffffull) return false;   // row coordinates are 32-bit
+    cuuint64_t dims[2] = {VD, rows};
+    cuuint64_t strides[1] = {VD * sizeof(float)};
+    cuuint32_t box[2] = {32, KD};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(pool), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
@@ -986,6 +1008,7 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
             !make_map(&p.to, a.o, a.H, a.T_total, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
+    if (!make_pool_map(&p.tpool, a.pool, a.num_slots, a.H)) return cudaErrorInvalidValue;
     p.N = a.N; p.T_total = a.T_total; p.H = a.H; p.num_slots = a.num_slots;
     p.beta = (const __nv_bfloat16 *)a.beta; p.cu = a.cu; p.pool = a.pool;
     p.init_slot = a.init_slot; p.out_slot = a.out_slot; p.snap_slot = a.snap_slot;
