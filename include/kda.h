@@ -425,6 +425,21 @@ KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems,
                           const int32_t *src, const int32_t *dst, int n, int32_t *dev_err,
                           void *stream);
 
+/*
+ * kda_selftest_bounded_wait -- exercises the bounded-wait path of the kernels.
+ *
+ * Launches one CTA that waits, with the wait loop the kernels use on their
+ * asynchronous copies, on a shared-memory barrier that nothing arrives at.
+ * The wait gives up after wait_us microseconds, sets KDA_DEVERR_TIMEOUT in
+ * *dev_err and the kernel returns: no fault, trap or hang, and the context
+ * stays usable.  Not part of the KDA path; it lets a test see the timeout
+ * status that a copy which never completes would produce.
+ *
+ *   dev_err  device int32 (required)
+ *   wait_us  1 .. 2,000,000
+ */
+KDA_API int kda_selftest_bounded_wait(int32_t *dev_err, int wait_us, void *stream);
+
 /* Human-readable name of a kda_status value. */
 KDA_API const char *kda_status_string(int status);
 

@@ -81,11 +81,12 @@ def lib() -> ctypes.CDLL:
                                        i, vp, f, f, f, ip, vp]
         L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
                                     i, ip, vp]
+        L.kda_selftest_bounded_wait.argtypes = [ip, i, vp]
         for fn in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step", "kda_verify_store_inputs",
                    "kda_verify_store_inputs_ragged", "kda_verify_snapshot",
                    "kda_snapshot_commit", "kda_conv_prologue", "kda_gated_rmsnorm",
                    "kda_decode_fused",
-                   "kda_replay_fold", "kda_slot_copy"):
+                   "kda_replay_fold", "kda_slot_copy", "kda_selftest_bounded_wait"):
             getattr(L, fn).restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -412,3 +413,11 @@ def kda_slot_copy(pools, src, dst, dev_err=None, stream=None):
     _check("kda_slot_copy", lib().kda_slot_copy(
         P, ptrs, slot_elems, pools[0].shape[0], _p(src), _p(dst), src.numel(), _p(dev_err),
         _stream(stream)))
+
+
+def kda_selftest_bounded_wait(dev_err, wait_us: int = 2000, stream=None):
+    """One CTA waits, with the kernels' bounded-wait loop, on a barrier nothing
+    arrives at; after wait_us it sets KDA_DEVERR_TIMEOUT in dev_err (a device
+    int32 tensor) and returns."""
+    _check("kda_selftest_bounded_wait", lib().kda_selftest_bounded_wait(_p(dev_err), int(wait_us),
+                                                                       _stream(stream)))

@@ -382,4 +382,9 @@ KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems,
     return from_cuda(kda::launch_slot_copy(p, (cudaStream_t)stream));
 }
 
+KDA_API int kda_selftest_bounded_wait(int32_t *dev_err, int wait_us, void *stream) {
+    if (!dev_err || wait_us < 1 || wait_us > 2000000) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_selftest_wait(dev_err, wait_us, (cudaStream_t)stream));
+}
+
 }  // extern "C"

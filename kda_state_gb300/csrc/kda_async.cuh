@@ -31,8 +31,8 @@ __device__ __forceinline__ void barrier_expect(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void barrier_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// Wait for the phase with the given parity; false after ASYNC_WAIT_NS.
-__device__ __forceinline__ bool barrier_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity; false after limit_ns.
+__device__ __forceinline__ bool barrier_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer();
     while (true) {
         uint32_t ok;
@@ -43,8 +43,11 @@ __device__ __forceinline__ bool barrier_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (global_timer() - t0 > ASYNC_WAIT_NS) return false;
+        if (global_timer() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool barrier_wait(uint32_t bar, uint32_t parity) {
+    return barrier_wait_for(bar, parity, ASYNC_WAIT_NS);
 }
 // bytes (a multiple of 16; both addresses 16-byte aligned) from global to
 // shared memory, completing on bar.

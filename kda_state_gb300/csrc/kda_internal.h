@@ -146,4 +146,7 @@ cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t s);
 // Chunked tensor-core prefill (bf16 inputs).
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s);
 
+// One CTA waiting on a barrier nothing arrives at, for wait_us microseconds.
+cudaError_t launch_selftest_wait(int32_t *err, int wait_us, cudaStream_t s);
+
 }  // namespace kda

@@ -206,3 +206,9 @@ def test_layout_helpers_match_page_sizes():
     for key in ("state_read_per_request_step_bytes", "state_per_request_tp8_bytes"):
         e = g[key]
         assert abs(e["layers"] * e["heads"] * sb - e["value"]) <= e["rel_tol"] * e["value"]
+
+
+def test_selftest_bounded_wait_rejects(L):
+    assert L.kda_selftest_bounded_wait(None, 1000, None) == -1              # no status word
+    assert L.kda_selftest_bounded_wait(FAKE, 0, None) == -1                 # limit below 1 us
+    assert L.kda_selftest_bounded_wait(FAKE, 2000001, None) == -1           # limit above 2 s
