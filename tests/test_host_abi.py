@@ -212,3 +212,25 @@ def test_selftest_bounded_wait_rejects(L):
     assert L.kda_selftest_bounded_wait(None, 1000, None) == -1              # no status word
     assert L.kda_selftest_bounded_wait(FAKE, 0, None) == -1                 # limit below 1 us
     assert L.kda_selftest_bounded_wait(FAKE, 2000001, None) == -1           # limit above 2 s
+
+
+def test_binding_rejects_host_tensors():
+    """Every wrapper checks its tensors before it touches the library: host
+    (CPU) tensors, which the C side would take as device pointers, raise."""
+    import kda_state_gb300 as kda
+    T, H, K = 4, 2, 128
+    x = {n: torch.zeros(T, H, K, dtype=torch.bfloat16) for n in ("q", "k", "v", "gk")}
+    beta = torch.zeros(T, H, dtype=torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    ids = torch.zeros(1, dtype=torch.int32)
+    pool = torch.zeros(1, H, K, K)
+    with pytest.raises(ValueError, match="q must be a CUDA tensor"):
+        kda.kda_chunk_prefill(x["q"], x["k"], x["v"], x["gk"], beta, cu, cu, pool, ids, ids)
+    with pytest.raises(ValueError, match="q must be a CUDA tensor"):
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["gk"], beta, ids, pool)
+    with pytest.raises(ValueError, match="pools\\[0\\] must be a CUDA tensor"):
+        kda.kda_slot_copy([pool], ids, ids)
+    with pytest.raises(ValueError, match="o must be a CUDA tensor"):
+        kda.kda_gated_rmsnorm(x["v"], x["v"], torch.zeros(K, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="dev_err must be a CUDA tensor"):
+        kda.kda_selftest_bounded_wait(torch.zeros(1, dtype=torch.int32))
