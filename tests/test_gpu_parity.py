@@ -78,6 +78,33 @@ def test_prefill_varlen_small(dtype, init_kind):
     assert torch.equal(pool[3 * N], r["before"][3 * N]), "untouched slot was written"
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_prefill_all_sequences_empty(dtype):
+    """A batch without tokens: each output and snapshot slot receives its
+    initial state bit for bit (zeros where init_slot is -1); nothing else is
+    written and o is empty."""
+    r = run_prefill_case([0, 0, 0], 2, dtype, "mixed", seed=13)
+    N, pool = r["N"], r["pool"]
+    assert r["o"].numel() == 0
+    want = torch.from_numpy(r["S_ref"]).float()
+    assert torch.equal(pool[N:2 * N].cpu(), want), "final states differ from the initial states"
+    assert torch.equal(pool[2 * N:3 * N].cpu(), want), "snapshots differ from the initial states"
+    assert torch.equal(pool[:N], r["before"][:N]), "checkpoint slots were written"
+    assert torch.equal(pool[3 * N], r["before"][3 * N]), "untouched slot was written"
+
+
+def test_decode_empty_batch_is_a_no_op():
+    """B = 0: the call succeeds, launches nothing and leaves the pool as it was."""
+    pool = canary_fill(torch.empty(2, 3, KD, VD, device=DEV))
+    before = pool.clone()
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=DEV)
+    o = kda().kda_decode_step(e(0, 3, KD), e(0, 3, KD), e(0, 3, VD), e(0, 3, KD), e(0, 3),
+                              torch.empty(0, dtype=torch.int32, device=DEV), pool)
+    torch.cuda.synchronize()
+    assert o.shape == (0, 3, VD)
+    assert torch.equal(pool, before)
+
+
 def test_tiny_config():
     """1 sequence, T = 64, H = 1, fp32, zero state, seed 0; the oracle's
     chunked form with chunk 64 gives the same reference."""
