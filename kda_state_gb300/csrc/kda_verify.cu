@@ -63,7 +63,7 @@ __device__ __forceinline__ void verify_unit_recurrent(const VerifyArgs &a, int b
 
 template <typename T>
 __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit - b * a.H;
     size_t tok0;
@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
     // path: registers, column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
     const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS;
     const int col = 16 * warp + (lane & 15), hr = lane >> 4;
-    const int g = lane >> 2, t4 = lane & 3;
     float s[TENSOR ? 1 : 64];
     const uint32_t bar = shared_addr(&sm.bar);
     if (tid == 0) {
@@ -382,43 +381,43 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
             return;
         }
         block_tensor_out<T>(sm, a, tok0, G, h, warp, lane);
-        return;
-    }
-    // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
-    // the other row half via one shuffle.  acc[i] (i < GM) is row i of W,
-    // acc[GM + i] row i of Q . E.
-    float acc[2 * GM];
+    } else {
+        // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
+        // the other row half via one shuffle.  acc[i] (i < GM) is row i of W,
+        // acc[GM + i] row i of Q . E.
+        float acc[2 * GM];
 #pragma unroll
-    for (int i = 0; i < 2 * GM; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 2 * GM; ++i) acc[i] = 0.f;
 #pragma unroll
-    for (int k4 = 0; k4 < 16; ++k4) {
-        const int k = 64 * hr + 4 * k4;
+        for (int k4 = 0; k4 < 16; ++k4) {
+            const int k = 64 * hr + 4 * k4;
 #pragma unroll
-        for (int i = 0; i < 2 * GM; ++i) {
-            if ((i < GM ? i : i - GM) < G) {
-                const float *row = (i < GM) ? sm.w[i] : sm.qg[i - GM];
-                const float4 x = *reinterpret_cast<const float4 *>(row + k);
-                acc[i] = fmaf(x.x, s[4 * k4], acc[i]);
-                acc[i] = fmaf(x.y, s[4 * k4 + 1], acc[i]);
-                acc[i] = fmaf(x.z, s[4 * k4 + 2], acc[i]);
-                acc[i] = fmaf(x.w, s[4 * k4 + 3], acc[i]);
+            for (int i = 0; i < 2 * GM; ++i) {
+                if ((i < GM ? i : i - GM) < G) {
+                    const float *row = (i < GM) ? sm.w[i] : sm.qg[i - GM];
+                    const float4 x = *reinterpret_cast<const float4 *>(row + k);
+                    acc[i] = fmaf(x.x, s[4 * k4], acc[i]);
+                    acc[i] = fmaf(x.y, s[4 * k4 + 1], acc[i]);
+                    acc[i] = fmaf(x.z, s[4 * k4 + 2], acc[i]);
+                    acc[i] = fmaf(x.w, s[4 * k4 + 3], acc[i]);
+                }
             }
         }
-    }
 #pragma unroll
-    for (int i = 0; i < 2 * GM; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
-    // U = U~ - W h0;  O = (Q . E) h0 + Aqk U;  each row half writes half the rows
-    float u[GM];
+        for (int i = 0; i < 2 * GM; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
+        // U = U~ - W h0;  O = (Q . E) h0 + Aqk U;  each row half writes half the rows
+        float u[GM];
 #pragma unroll
-    for (int r = 0; r < GM; ++r) u[r] = (r < G) ? sm.ut[r][col] - acc[r] : 0.f;
-    const int half = (G + 1) / 2;
+        for (int r = 0; r < GM; ++r) u[r] = (r < G) ? sm.ut[r][col] - acc[r] : 0.f;
+        const int half = (G + 1) / 2;
 #pragma unroll
-    for (int r = 0; r < GM; ++r) {
-        if (r < G && ((r < half) == (hr == 0))) {
-            float o = acc[GM + r];
+        for (int r = 0; r < GM; ++r) {
+            if (r < G && ((r < half) == (hr == 0))) {
+                float o = acc[GM + r];
 #pragma unroll
-            for (int j = 0; j <= r; ++j) o = fmaf(sm.aqk[r][j], u[j], o);
-            ((T *)a.o)[((tok0 + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
+                for (int j = 0; j <= r; ++j) o = fmaf(sm.aqk[r][j], u[j], o);
+                ((T *)a.o)[((tok0 + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
+            }
         }
     }
 }
