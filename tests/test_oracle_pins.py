@@ -365,6 +365,76 @@ MUTANTS = {
 }
 
 
+# mistakes in the packed-batch bookkeeping of the C source (every access stays
+# in bounds, so a mutant fails a pin instead of crashing the test process)
+MUTANTS.update({
+    "batch_beta_token_stride": ("long sk = (long)J->H * J->K, sv = (long)J->H * J->V, sb = J->H;",
+                                "long sk = (long)J->H * J->K, sv = (long)J->H * J->V, sb = 1;"),
+    "batch_output_head_offset_dropped": ("double *o = J->o ? J->o + t0 * sv + (long)h * J->V : NULL;",
+                                         "double *o = J->o ? J->o + t0 * sv : NULL;"),
+    "batch_states_reversed": ("double *S = J->S + (size_t)u * J->K * J->V;",
+                              "double *S = J->S + (size_t)(J->n_units - 1 - u) * J->K * J->V;"),
+    "batch_gate_from_key": ("const double *gk = J->gk + t0 * sk + (long)h * J->K;",
+                            "const double *gk = J->k + t0 * sk + (long)h * J->K;"),
+})
+
+# mistakes in the Python drivers (oracle/__init__.py), run against the same
+# C library
+PY_MUTANTS = {
+    "fold_one_record_too_many": ("    Tn = np.repeat(acc, H)\n",
+                                 "    Tn = np.repeat(np.minimum(acc + 1, G), H)\n"),
+    "verify_writes_committed_state": (
+        "    S = _f64(S0).reshape(B * H, *S0.shape[2:]).copy()   # scratch copy: S0 untouched\n"
+        "    tok0 = np.repeat(np.arange(B) * G, H)",
+        "    S = _f64(S0).reshape(B * H, *S0.shape[2:])\n"
+        "    tok0 = np.repeat(np.arange(B) * G, H)"),
+    "checkpoint_index_off_by_one": ("            m = start // interval\n",
+                                    "            m = start // interval + 1\n"),
+    "ragged_last_draft_dropped": (
+        "    o, _ = _batch(tok0, np.repeat(cu[1:] - cu[:-1], H), head,",
+        "    o, _ = _batch(tok0, np.repeat(np.maximum(cu[1:] - cu[:-1] - 1, 0), H), head,"),
+    "varlen_state_to_next_sequence": ("    Sout = S0.copy()\n    for i, (n, h) in enumerate(units):\n"
+                                      "        Sout[n, h] = S[i]\n    return o, Sout\n",
+                                      "    Sout = S0.copy()\n    for i, (n, h) in enumerate(units):\n"
+                                      "        Sout[(n + 1) % N, h] = S[i]\n    return o, Sout\n"),
+}
+
+
+def _failed_pins(orc):
+    failed = []
+    for pin in PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+def _driver_copy(old=None, new=None, name="copy"):
+    """A fresh copy of the oracle's Python drivers, with one text substitution."""
+    import types
+    path = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+    src = open(path).read()
+    if old is not None:
+        assert src.count(old) == 1, "mutation anchor not found: %s" % name
+        src = src.replace(old, new, 1)
+    ns = {"__file__": path, "__name__": "oracle_%s" % name}
+    exec(compile(src, path, "exec"), ns)
+    return types.SimpleNamespace(**{f: ns[f] for f in ("unit", "prefill_varlen", "prefill_checkpoints",
+                                                       "decode", "verify", "verify_ragged", "fold")})
+
+
+def test_unmutated_driver_copy_passes_every_pin():
+    """Control for the driver mutants: the copy loaded the same way passes."""
+    assert _failed_pins(_driver_copy()) == []
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pins_catch_planted_driver_mistakes(name):
+    old, new = PY_MUTANTS[name]
+    assert _failed_pins(_driver_copy(old, new, name)), "planted mistake %s passed every pin" % name
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistakes(name, tmp_path):
     if shutil.which("gcc") is None:
@@ -375,10 +445,4 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
     mpath = tmp_path / ("mut_%s.c" % name)
     mpath.write_text(src.replace(old, new, 1))
     mut = oracle.load_variant(str(mpath), str(tmp_path / ("mut_%s.so" % name)))
-    failed = []
-    for pin in PINS:
-        try:
-            pin(mut)
-        except AssertionError:
-            failed.append(pin.__name__)
-    assert failed, "planted mistake %s passed every pin" % name
+    assert _failed_pins(mut), "planted mistake %s passed every pin" % name
