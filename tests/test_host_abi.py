@@ -187,6 +187,36 @@ def test_slot_copy_rejects(L):
     assert L.kda_slot_copy(1, pools, 16, 4, None, None, 0, None, None) == 0      # nothing to copy
 
 
+def test_size_and_alignment_limits_reject(L):
+    """The remaining host checks, each met with every earlier check passing, so
+    each call is refused by the check named beside it (nothing is launched)."""
+    MIS = ctypes.c_void_p(4100)                    # not 16-byte aligned
+    cu = _cu([0, 5, 9])
+    pre = lambda H, q: (0, 2, 9, H, 128, 128, q, FAKE, FAKE, FAKE, FAKE, FAKE, cu, FAKE, 4, FAKE,
+                        FAKE, None, FAKE, 1.0, None, None)
+    assert L.kda_chunk_prefill(*pre(2, MIS)) == -1                  # bf16 q not 16-byte aligned
+    assert L.kda_chunk_prefill(*pre((1 << 30) + 1, FAKE)) == -1     # N * H beyond 32 bits
+    assert L.kda_chunk_prefill(*pre(0, FAKE)) == -1                 # H < 1
+    dec = lambda B, H: (0, B, H, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 1.0,
+                        None, None)
+    assert L.kda_decode_step(*dec(1 << 16, 1 << 16)) == -1          # B * H beyond 32 bits
+    assert L.kda_decode_step(*dec(4, 0)) == -1                      # H < 1
+    import kda_state_gb300 as kda
+    ring = kda.kda_ring(4096, 4096, 4096, 4096, 256, 0)
+    assert L.kda_verify_store_inputs(0, 2, 65, 2, 128, 128, *(FAKE,) * 6, FAKE, 4,
+                                     ctypes.byref(ring), None, FAKE, 1.0, None, None) == -1   # G > 64
+    rings = (kda.kda_ring * 2)(kda.kda_ring(4096, 4096, 4096, 4096, 16, 0),
+                               kda.kda_ring(4096, 4096, 4096, 4096, 16, 0))
+    for bad in (None, 4100):                                        # a null / misaligned pool
+        pools = (ctypes.c_void_p * 2)(4096, bad)
+        assert L.kda_replay_fold(0, 2, 2, 2, 128, 128, pools, rings, 4, 8, FAKE, FAKE, None, None,
+                                 None) == -1
+    pro = lambda H, stride: (0, 2, 9, H, 128, FAKE, FAKE, FAKE, stride, FAKE, FAKE, FAKE, 4, FAKE,
+                             FAKE, FAKE, cu, FAKE, FAKE, FAKE, FAKE, 1e-6, None, None)
+    assert L.kda_conv_prologue(*pro(2, 260)) == -1                  # stride not a multiple of 8
+    assert L.kda_conv_prologue(*pro(65536, 65536 * 128)) == -1      # H > 65535 (the entry point's limit)
+
+
 def test_layout_helpers_match_page_sizes():
     import kda_state_gb300 as kda
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "page_sizes.json")))
