@@ -1,0 +1,48 @@
+"""Host logic of bench.py that decides what the JSON line reports: the kernel
+source hash (source file plus the device headers it includes, in include
+order) and the rule that a profile's DRAM traffic is reported only while the
+profile was taken on the current source."""
+import os
+import shutil
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.fixture
+def tree(tmp_path, monkeypatch):
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cu").write_text('#include "a.cuh"\n#include <cuda.h>\nint k;\n')
+    (csrc / "a.cuh").write_text('#include "b.cuh"\nint a;\n')
+    (csrc / "b.cuh").write_text('#include "a.cuh"\nint b;\n')      # cycle: visited once
+    monkeypatch.setattr(bench, "CSRC", str(csrc))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    return tmp_path
+
+
+def test_device_headers_in_include_order(tree):
+    assert bench._device_headers("k.cu", []) == ["a.cuh", "b.cuh"]
+
+
+def test_source_hash_covers_included_headers(tree):
+    h0 = bench.source_sha1("k.cu")
+    assert len(h0) == 12 and h0 == bench.source_sha1("k.cu")
+    (tree / "csrc" / "b.cuh").write_text('#include "a.cuh"\nint b2;\n')
+    assert bench.source_sha1("k.cu") != h0
+
+
+def test_profile_traffic_only_for_the_current_source(tree):
+    prof = tree / "profiles" / "k.md"
+    assert bench.profile_traffic("k.cu", "k.md") is None                  # no summary
+    prof.write_text("source_sha1: %s\ndram_bytes_per_launch: 1234567\n" % bench.source_sha1("k.cu"))
+    assert bench.profile_traffic("k.cu", "k.md") == 1234567.0
+    (tree / "csrc" / "a.cuh").write_text('#include "b.cuh"\nint a_changed;\n')
+    assert bench.profile_traffic("k.cu", "k.md") is None                  # source changed since
+    prof.write_text("source_sha1: %s\n" % bench.source_sha1("k.cu"))
+    assert bench.profile_traffic("k.cu", "k.md") is None                  # no traffic recorded
