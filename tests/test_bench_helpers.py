@@ -46,3 +46,23 @@ def test_profile_traffic_only_for_the_current_source(tree):
     assert bench.profile_traffic("k.cu", "k.md") is None                  # source changed since
     prof.write_text("source_sha1: %s\n" % bench.source_sha1("k.cu"))
     assert bench.profile_traffic("k.cu", "k.md") is None                  # no traffic recorded
+
+
+def test_clock_summary_uses_the_timed_window():
+    """Median SM clock and throttle reasons come from the samples taken between
+    the two marks (the timed region); unreadable fields are skipped."""
+    c = bench.ClockSampler(0)
+    row = lambda sm, reasons: [sm, "2070", "900.0", "0x0"] + reasons
+    idle = ["Not Active"] * 4
+    c.samples = [(0.5, row("1200", ["Active", "Active", "Not Active", "Not Active"])),   # before
+                 (1.5, row("2070", idle)), (2.0, row("2010", idle)),
+                 (2.5, row("[N/A]", ["Not Active", "Not Active", "Not Active", "Active"])),
+                 (3.5, row("900", ["Not Active", "Not Active", "Active", "Not Active"]))]  # after
+    c.marks = [1.0, 3.0]
+    s = c.summary()
+    assert s["sm_mhz"] == 2040.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    c.marks = []                                       # no marks: every sample counts
+    assert c.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap",
+                                      "sw_thermal_slowdown"]
+    assert bench.ClockSampler(0).summary()["reasons"] == ["no samples"]
