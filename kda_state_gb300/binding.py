@@ -4,6 +4,14 @@ Argument marshalling only -- every step of the KDA path runs in the library's
 CUDA kernels.  Tensors are torch tensors on the current CUDA device (PyTorch
 supplies device memory and streams); shapes follow include/kda.h.  If the
 library is missing the calls raise: there is no other implementation.
+
+Errors that depend on device data (a slot id out of range, inconsistent
+cu_seqlens, an accept length above the window, a wait that gave up) are found
+by the kernels, which skip the affected unit and set KDA_DEVERR_* bits in
+``dev_err``.  The calls never synchronise, so those bits cannot be raised here:
+pass a zeroed int32 device tensor as ``dev_err`` and read it after the stream
+has synchronised.  With ``dev_err=None`` (the default) such units are skipped
+without a report.
 """
 from __future__ import annotations
 

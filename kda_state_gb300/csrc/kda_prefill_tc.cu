@@ -865,7 +865,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         if (c + 1 < nchunks && !mbar_wait(bar_qkg, par ^ 1u)) atomicOr(flags, FLAG_TIMEOUT);
         load_raw();
         mma_wait_all(bar_mma, 1, flags);
-        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+        const int fl = *flags;   // uniform: read after the barrier, before this phase sets bits
+        if (fl & FLAG_TIMEOUT) { aborted = true; break; }
         // (11) the state update (O is written out during the next chunk's solve)
         {
             // two 16-column reads keep the next chunk's raw tiles in registers
@@ -884,7 +885,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             if (absmax(S, 32) > FP16_LIMIT) atomicOr(flags, FLAG_RANGE);
             // the exact state after (m + 1) * ckpt_chunks full chunks
             const int m = (c + 1) / max(p.ckpt_chunks, 1) - 1;
-            if (nck > 0 && (c + 1) % p.ckpt_chunks == 0 && m < nck && !(*flags & FLAG_TIMEOUT)) {
+            if (nck > 0 && (c + 1) % p.ckpt_chunks == 0 && m < nck && !(fl & FLAG_RANGE)) {
                 const int cs = p.ckpt_slots[(size_t)n * p.max_ckpts + m];
                 if (cs >= 0) {
                     float4 *dst = reinterpret_cast<float4 *>(
@@ -913,10 +914,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         store_o(p, tmem, lq, cq, lane, tl, eos - tl, h);
     }
 
-    if ((*flags & FLAG_RANGE) && tid == 0) report(p.err, DEVERR_RANGE);
+    const bool range = (*flags & FLAG_RANGE) != 0;
+    if (range && tid == 0) report(p.err, DEVERR_RANGE);
     if (aborted) {
         if (tid == 0) report(p.err, DEVERR_TIMEOUT);
-    } else {   // aborted is uniform; no copy or MMA is in flight, all of shared memory is free
+    } else if (!range) {   // uniform; no copy or MMA is in flight, all of shared memory is free
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             *reinterpret_cast<float4 *>(stg + srow * VD + 4 * ((8 * cq + j) ^ (srow & 7))) =

@@ -233,7 +233,7 @@ def test_decode_full_layer():
 def test_verify_fold_full():
     """64 requests x 8 draft tokens, 69 layers x H = 64, 128-slot pools, ring
     16, accept lengths 1..8 (mean about 2.7): 69 verify launches then one fold
-    over all layers.  Committed states untouched by verify; sampled layers'
+    over all layers.  Committed states untouched by verify; every layer's
     fold bit-identical to repeated decode; sampled units vs the oracle."""
     B, G, H, S, R, Lyr = 64, 8, 64, 128, 16, 69
     g = gen.make_gen(4)
@@ -259,15 +259,18 @@ def test_verify_fold_full():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     reqs = [0, 17, 63]
-    for l in (0, 34, 68):
+    ref = torch.empty_like(pools[0])
+    for l in range(Lyr):
         x = xs[l]
-        ref = committed[l].clone()
+        ref.copy_(committed[l])
         for i in range(G):
             sel = (accept > i).nonzero().flatten().to(DEV)
             kda().kda_decode_step(*(x[n][sel, i].contiguous() for n in ("q", "k", "v", "gk", "beta")),
                                   idd[sel].contiguous(), ref)
         torch.cuda.synchronize()
         assert torch.equal(pools[l], ref), "fold differs from repeated decode, layer %d" % l
+        if l not in (0, 34, 68):
+            continue
         rs = torch.tensor(reqs, device=DEV)
         xh = {n: f64(t[rs]) for n, t in x.items()}
         S0 = f64(committed[l][idd[rs].long()])
