@@ -77,11 +77,10 @@ enum {
     KDA_DEVERR_ACCEPT_RANGE = 2, /* an accept length outside [0, max_accept] */
     KDA_DEVERR_SEQLENS = 4,      /* cu_seqlens or cu_drafts not monotone or past total_tokens,
                                     or a draft count above G_max */
-    KDA_DEVERR_RANGE = 8,        /* chunked prefill: a key channel's log-decay summed over half a
-                                    chunk (32 tokens) is below -85, or a chunk intermediate
-                                    (state, W, U) exceeds 60000 in magnitude: outside what the
-                                    kernel's operand formats represent; that unit's outputs and
-                                    state are not valid */
+    KDA_DEVERR_RANGE = 8,        /* reserved: no kernel sets it.  The chunked prefill runs any
+                                    chunk whose values leave its tensor-core operand formats
+                                    (strong decays, positive gk, large q, k, v or state) through
+                                    an exact fp32 recurrence instead of reporting it */
     KDA_DEVERR_TIMEOUT = 16      /* a kernel's bounded wait on its own copies gave up (the unit
                                     is abandoned, its slot is not written) */
 };
@@ -145,6 +144,12 @@ typedef struct {
  *   stream          cudaStream_t
  * bf16 runs the chunked tensor-core kernel; fp32 runs an exact fp32 kernel on
  * the CUDA cores.  Zero-length sequences copy init to out (or write zeros).
+ * The chunked kernel is defined on every input the recurrence is: a chunk
+ * whose decays or magnitudes leave its operand formats (a key channel's
+ * log-decay over half a chunk beyond 80 in magnitude, a positive gk, |q| or
+ * |k| above 256, |v| or an intermediate above 60000) is computed by the exact
+ * recurrence in fp32 instead, slower but within the same tolerance.  A unit
+ * whose bounded wait gave up (KDA_DEVERR_TIMEOUT) writes none of its slots.
  */
 KDA_API int kda_chunk_prefill(kda_dtype dt, int num_seqs, int total_tokens, int H, int K, int V,
                               const void *q, const void *k, const void *v, const void *gk,
@@ -439,6 +444,28 @@ KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems,
  *   wait_us  1 .. 2,000,000
  */
 KDA_API int kda_selftest_bounded_wait(int32_t *dev_err, int wait_us, void *stream);
+
+/*
+ * kda_selftest_prefill_wait -- exercises the chunked prefill's own bounded wait.
+ *
+ * Runs the bf16 chunked prefill kernel (the kernel kda_chunk_prefill launches)
+ * on the given batch, except that the first chunk's q, k and gk tiles are never
+ * requested, so the first wait of every unit is on a barrier nothing arrives
+ * at.  Each unit's waits give up after wait_us microseconds: KDA_DEVERR_TIMEOUT
+ * is set in *dev_err, the unit writes no slot (out_slot keeps its contents),
+ * frees its tensor memory and returns.  No fault, trap or hang; the context
+ * stays usable and the next launch runs normally.  Not part of the KDA path.
+ *
+ *   arguments as kda_chunk_prefill (dtype bf16, K = V = 128, no snapshot,
+ *   scale 1); total_tokens >= 1; dev_err required; wait_us 1 .. 2,000,000
+ */
+KDA_API int kda_selftest_prefill_wait(int num_seqs, int total_tokens, int H, const void *q,
+                                      const void *k, const void *v, const void *gk,
+                                      const void *beta, const int32_t *cu_seqlens_dev,
+                                      const int32_t *cu_seqlens_host, float *state_pool,
+                                      int num_slots, const int32_t *init_slot,
+                                      const int32_t *out_slot, void *o, int32_t *dev_err,
+                                      int wait_us, void *stream);
 
 /* Human-readable name of a kda_status value. */
 KDA_API const char *kda_status_string(int status);

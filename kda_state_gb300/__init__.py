@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     kda_replay_fold,
     kda_ring,
     kda_selftest_bounded_wait,
+    kda_selftest_prefill_wait,
     kda_slot_copy,
     kda_snapshot_commit,
     kda_status_string,

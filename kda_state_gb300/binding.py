@@ -90,11 +90,14 @@ def lib() -> ctypes.CDLL:
         L.kda_slot_copy.argtypes = [i, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, i, ip, ip,
                                     i, ip, vp]
         L.kda_selftest_bounded_wait.argtypes = [ip, i, vp]
+        L.kda_selftest_prefill_wait.argtypes = [i, i, i, vp, vp, vp, vp, vp, ip, ip, vp, i, ip, ip,
+                                                vp, ip, i, vp]
         for fn in ("kda_chunk_prefill", "kda_chunk_prefill_checkpoints", "kda_decode_step", "kda_verify_store_inputs",
                    "kda_verify_store_inputs_ragged", "kda_verify_snapshot",
                    "kda_snapshot_commit", "kda_conv_prologue", "kda_gated_rmsnorm",
                    "kda_decode_fused",
-                   "kda_replay_fold", "kda_slot_copy", "kda_selftest_bounded_wait"):
+                   "kda_replay_fold", "kda_slot_copy", "kda_selftest_bounded_wait",
+                   "kda_selftest_prefill_wait"):
             getattr(L, fn).restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -610,3 +613,30 @@ def kda_selftest_bounded_wait(dev_err, wait_us: int = 2000, stream=None):
         raise ValueError("dev_err needs at least one element")
     _check("kda_selftest_bounded_wait", lib().kda_selftest_bounded_wait(_p(dev_err), int(wait_us),
                                                                        _stream(stream)))
+
+
+def kda_selftest_prefill_wait(q, k, v, gk, beta, cu_seqlens, cu_seqlens_host, state_pool,
+                              init_slot, out_slot, dev_err, o=None, wait_us: int = 1000,
+                              stream=None):
+    """The bf16 chunked prefill with the first chunk's q, k, gk never requested:
+    every unit's first wait gives up after wait_us, sets KDA_DEVERR_TIMEOUT in
+    dev_err and the unit writes no slot.  Arguments as ``kda_chunk_prefill``
+    (bf16 only).  Returns o (not written by the abandoned units)."""
+    _need(q, "q", (None, None, None), dtype=torch.bfloat16)
+    T = q.shape[0]
+    dt, dev, H, K, V = _need_inputs(q, k, v, gk, beta, (T,))
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    N = host.numel() - 1
+    _need_prefill_common(cu_seqlens, N, state_pool, H, K, V, init_slot, out_slot, None, dev_err,
+                         dev)
+    if dev_err is None:
+        raise ValueError("dev_err is required")
+    if o is None:
+        o = torch.empty(T, H, V, dtype=q.dtype, device=q.device)
+    _need(o, "o", (T, H, V), dt, dev)
+    hp = host.numpy().ctypes.data_as(ctypes.c_void_p)
+    _check("kda_selftest_prefill_wait", lib().kda_selftest_prefill_wait(
+        N, T, H, _p(q), _p(k), _p(v), _p(gk), _p(beta), _p(cu_seqlens), hp, _p(state_pool),
+        state_pool.shape[0], _p(init_slot), _p(out_slot), _p(o), _p(dev_err), int(wait_us),
+        _stream(stream)))
+    return o

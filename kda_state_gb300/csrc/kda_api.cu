@@ -34,7 +34,8 @@ static int prefill_impl(kda_dtype dt, int num_seqs, int total_tokens, int H, int
                         const int32_t *cu_seqlens_host, float *state_pool, int num_slots,
                         const int32_t *init_slot, const int32_t *out_slot,
                         const int32_t *snap_slot, int ckpt_interval, const int32_t *ckpt_slots,
-                        int max_ckpts, void *o, float scale, int32_t *dev_err, void *stream) {
+                        int max_ckpts, void *o, float scale, int32_t *dev_err, void *stream,
+                        uint64_t wait_ns = 0, int skip_first_load = 0) {
     if (!dtype_ok(dt)) return KDA_ERR_UNSUPPORTED;
     if (!dims_ok(K, V)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || num_slots < 1 || !isfinite(scale))
@@ -57,6 +58,7 @@ static int prefill_impl(kda_dtype dt, int num_seqs, int total_tokens, int H, int
     a.pool = state_pool; a.init_slot = init_slot; a.out_slot = out_slot; a.snap_slot = snap_slot;
     a.o = o; a.scale = scale; a.err = dev_err;
     a.ckpt_interval = ckpt_interval; a.max_ckpts = max_ckpts; a.ckpt_slots = ckpt_slots;
+    a.wait_ns = wait_ns; a.skip_first_load = skip_first_load;
     cudaStream_t s = (cudaStream_t)stream;
     if (dt == KDA_DTYPE_BF16) {
         // the tensor-core kernel stages q, k, v, gk with TMA and stores o in 16-byte vectors
@@ -380,6 +382,20 @@ KDA_API int kda_slot_copy(int num_pools, float *const *pools, size_t slot_elems,
     p.src = src; p.dst = dst; p.err = dev_err;
     for (int i = 0; i < num_pools; ++i) p.pool[i] = pools[i];
     return from_cuda(kda::launch_slot_copy(p, (cudaStream_t)stream));
+}
+
+KDA_API int kda_selftest_prefill_wait(int num_seqs, int total_tokens, int H, const void *q,
+                                      const void *k, const void *v, const void *gk,
+                                      const void *beta, const int32_t *cu_seqlens_dev,
+                                      const int32_t *cu_seqlens_host, float *state_pool,
+                                      int num_slots, const int32_t *init_slot,
+                                      const int32_t *out_slot, void *o, int32_t *dev_err,
+                                      int wait_us, void *stream) {
+    if (!dev_err || wait_us < 1 || wait_us > 2000000 || total_tokens < 1) return KDA_ERR_INVALID_ARG;
+    return prefill_impl(KDA_DTYPE_BF16, num_seqs, total_tokens, H, 128, 128, q, k, v, gk, beta,
+                        cu_seqlens_dev, cu_seqlens_host, state_pool, num_slots, init_slot, out_slot,
+                        nullptr, 0, nullptr, 0, o, 1.0f, dev_err, stream,
+                        (uint64_t)wait_us * 1000ull, 1);
 }
 
 KDA_API int kda_selftest_bounded_wait(int32_t *dev_err, int wait_us, void *stream) {

@@ -71,6 +71,8 @@ struct PrefillArgs {
     int ckpt_interval;             // 0: no checkpoints
     int max_ckpts;
     const int32_t *ckpt_slots;     // device [N][max_ckpts]
+    uint64_t wait_ns = 0;          // limit of the kernel's waits (0: its default)
+    int skip_first_load = 0;       // self-test only: the first chunk's q, k, gk are never requested
 };
 
 // Snapshot-per-step verify: the state after every draft step into a

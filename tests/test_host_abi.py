@@ -244,6 +244,16 @@ def test_selftest_bounded_wait_rejects(L):
     assert L.kda_selftest_bounded_wait(FAKE, 2000001, None) == -1           # limit above 2 s
 
 
+def test_selftest_prefill_wait_rejects(L):
+    cu = (ctypes.c_int32 * 2)(0, 4)
+    args = lambda err, us, T=4: (1, T, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cu, FAKE, 2, FAKE, FAKE,
+                                 FAKE, err, us, None)
+    assert L.kda_selftest_prefill_wait(*args(None, 1000)) == -1       # no status word
+    assert L.kda_selftest_prefill_wait(*args(FAKE, 0)) == -1          # limit below 1 us
+    assert L.kda_selftest_prefill_wait(*args(FAKE, 2000001)) == -1    # limit above 2 s
+    assert L.kda_selftest_prefill_wait(*args(FAKE, 1000, T=0)) == -1  # no token to wait for
+
+
 def test_binding_rejects_host_tensors():
     """Every wrapper checks its tensors before it touches the library: host
     (CPU) tensors, which the C side would take as device pointers, raise."""
