@@ -84,7 +84,11 @@ constexpr uint32_t RAW_Q = 0;          // 64 tokens x 128 ch bf16, 2 boxes of 64
 constexpr uint32_t RAW_K = 16384;
 constexpr uint32_t RAW_G = 32768;
 constexpr uint32_t SCR_A = 49152;      // fp32 A [64][AS]
-constexpr uint32_t OP_TBZ = 69632;     // rows 0-63 T Diag(b) (bf16), 64-127 zero, 128-191 Aqk (fp16)
+// [T Diag(b); Aqk] (fp16, K-major, 64 token columns): the A operand of both U
+// and O.  U = [T Diag(b); Aqk] V' keeps rows 0-63 (its rows 64-127, Aqk V', are
+// never read), and O = [T Diag(b); Aqk] U added onto P keeps rows 64-127 (its
+// rows 0-63 land on K~ S0, which is no longer needed), so no zero rows are kept.
+constexpr uint32_t OP_TBZ = 69632;
 constexpr uint32_t SCR_RW = 94208;     // per-warp R scratch of the solve (6 x 16 x RW floats)
 constexpr uint32_t R1_END = 98304;
 // The recurrent path (a chunk outside the operand formats) reuses the solve
@@ -94,9 +98,9 @@ constexpr uint32_t FB_IN = SCR_A;            // 2 x {alpha, k, q, v}[128] fp32
 constexpr uint32_t FB_P = SCR_A + 4096;      // [4 pk | 4 pq][128] fp32
 constexpr uint32_t FB_X = SCR_A + 8192;      // [2][4] k.q partials, [2] beta
 constexpr int FB_LD = 129;                   // row stride (floats) of the staged state
-constexpr uint32_t RAW_V = 98304;      // v, bf16, also the MN-major B operand of U~ = T Diag(b) V
-constexpr uint32_t OP_KT = 114688;     // K . exp(G), bf16, 64 tokens x 128 ch, MN-major B
-constexpr uint32_t OP_A3 = 131072;     // [-W; Q . exp(G)], fp16, 128 rows x 128 ch, K-major A
+constexpr uint32_t RAW_V = 98304;      // v (bf16, TMA), then V' = V - K~ S0 in place (fp16): MN-major B of U
+constexpr uint32_t OP_OST = 114688;    // staging of the previous chunk's O for its tensor store (8 x 2 KB)
+constexpr uint32_t OP_A3 = 131072;     // [K~; Q~] = [K; Q] . exp(G), fp16, 128 rows x 128 ch, K-major A of P
 constexpr uint32_t OP_S = 163840;      // S0, fp16, 128 rows (k) x 128 (v), MN-major B
 constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 128 ch, MN-major A
 constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
@@ -107,21 +111,26 @@ constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
 // row with its 16-byte chunks XOR-swizzled by (row & 7).  Out: rows of 512
 // bytes, chunks XOR-swizzled by (row & 7), stored as whole rows.  Either way
 // each thread's 128-byte row segment moves without bank conflicts.
-constexpr uint32_t STG = OP_KT;
+constexpr uint32_t STG = OP_OST;
 constexpr uint32_t SM_BETA = 229376;   // fp32 [64]
 constexpr uint32_t SM_GAM = SM_BETA + 256;   // fp32 [2][128]: exp(G_L), by chunk parity
-constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 4 mbarriers
+constexpr uint32_t SM_BAR = SM_GAM + 1024;   // 5 mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 64;    // TMEM base, flags
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 static_assert(SCR_A + 64 * AS * 4 <= OP_TBZ, "solve scratch overlaps the TBZ tile");
-static_assert(OP_TBZ + 192 * 128 <= SCR_RW && SCR_RW + 6 * 16 * 8 * 4 <= R1_END, "R scratch misplaced");
-static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 192 * 128 <= R1_END, "TBZ tile misplaced");
+static_assert(OP_TBZ + 128 * 128 <= SCR_RW && SCR_RW + 6 * 16 * 8 * 4 <= R1_END, "R scratch misplaced");
+static_assert(OP_TBZ % 1024 == 0 && OP_TBZ + 128 * 128 <= R1_END, "TBZ tile misplaced");
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 static_assert(FB_X + 64 <= SCR_A + 64 * AS * 4, "recurrent scratch overflows the solve scratch");
 static_assert(STG + 128 * FB_LD * 4 <= OP_KE, "staged state overlaps K_end");
 
-constexpr uint32_t TMEM_COLS = 256;
+// TMEM columns (512 allocated; one CTA per SM): the Gram product, then U,
+// then the state increment share columns 0..127; P = [K~; Q~] S0 of a chunk
+// (rows 64..127 becoming its O) lives in columns 256..383 or 384..511 by
+// chunk parity, so that the previous chunk's O survives the next P.
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_P = 256;
 constexpr uint64_t WAIT_NS = 2000000000ull;   // bounded waits: 2 s
 constexpr float FP16_LIMIT = 60000.f;         // fp16 operands must stay below this
 constexpr float QK_LIMIT = 256.f;             // |q|, |k| bound of the tensor-core path
@@ -294,11 +303,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ void store_bf16(uint8_t *base, uint32_t off, const float *v8) {
-    *reinterpret_cast<uint4 *>(base + off) =
-        make_uint4(pack_bf16x2(v8[0], v8[1]), pack_bf16x2(v8[2], v8[3]),
-                   pack_bf16x2(v8[4], v8[5]), pack_bf16x2(v8[6], v8[7]));
-}
 __device__ __forceinline__ void store_f16(uint8_t *base, uint32_t off, const float *v8) {
     *reinterpret_cast<uint4 *>(base + off) =
         make_uint4(pack_f16x2(v8[0], v8[1]), pack_f16x2(v8[2], v8[3]), pack_f16x2(v8[4], v8[5]),
@@ -366,20 +370,24 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 }
 constexpr int RW = 8;    // row stride (floats) of a warp's 16 x 8 R scratch
 
-// T Diag(beta) element pair (r, c), (r, c + 1), c even, as bf16 into the
-// K-major [T Diag(b); 0; Aqk] tile (64 token columns, one 128-byte row per r).
-__device__ __forceinline__ void store_tb2(uint8_t *tbz, int r, int c, float t0, float t1,
-                                          const float *beta) {
+// T Diag(beta) element pair (r, c), (r, c + 1), c even, as fp16 into the
+// K-major [T Diag(b); 0; Aqk] tile (64 token columns, one 128-byte row per r);
+// returns the larger magnitude (NaN if either is NaN).
+__device__ __forceinline__ float store_tb2(uint8_t *tbz, int r, int c, float t0, float t1,
+                                           const float *beta) {
+    const float a = t0 * beta[c], b = t1 * beta[c + 1];
     *reinterpret_cast<uint32_t *>(tbz + r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2) =
-        pack_bf16x2(t0 * beta[c], t1 * beta[c + 1]);
+        pack_f16x2(a, b);
+    return maxnan3(0.f, fabsf(a), fabsf(b));
 }
 
 template <int J>
-__device__ __forceinline__ void solve_block_column(const float *As, float *Ts, float *Rw, int lane,
+__device__ __forceinline__ float solve_block_column(const float *As, float *Ts, float *Rw, int lane,
                                                    uint8_t *tbz, const float *beta, int nt) {
     // This warp owns the 8 columns 16J + 8nt .. +7 of block column J; the two
     // halves of a block column never read each other's results.
     const int g = lane >> 2, t4 = lane & 3;
+    float bound = 0.f;
 #pragma unroll
     for (int I = J + 1; I < 4; ++I) {
         float rc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -417,19 +425,21 @@ __device__ __forceinline__ void solve_block_column(const float *As, float *Ts, f
         Ts[(16 * I + g) * 64 + c + 1] = -tc[1];
         Ts[(16 * I + g + 8) * 64 + c] = -tc[2];
         Ts[(16 * I + g + 8) * 64 + c + 1] = -tc[3];
-        store_tb2(tbz, 16 * I + g, cl, -tc[0], -tc[1], beta);
-        store_tb2(tbz, 16 * I + g + 8, cl, -tc[2], -tc[3], beta);
+        bound = maxnan3(bound, store_tb2(tbz, 16 * I + g, cl, -tc[0], -tc[1], beta),
+                        store_tb2(tbz, 16 * I + g + 8, cl, -tc[2], -tc[3], beta));
         __syncwarp();
     }
+    return bound;
 }
 
-// O of a chunk, from rows 64..127 of TMEM columns 128..255: this warp's lane
-// quarter lq (2 or 3) and columns 32 cq .. 32 cq + 31, scaled, rounded to bf16
-// and stored for the chunk's first L tokens (the chunk starts at token t0).
-__device__ __forceinline__ void store_o(const Params &p, uint32_t tmem, int lq, int cq, int lane, int t0,
-                                        int L, int h) {
+// O of a chunk, from rows 64..127 of its P columns (TMEM column ocol on):
+// this warp's lane quarter lq (2 or 3) and columns 32 cq .. 32 cq + 31, scaled,
+// rounded to bf16 and stored for the chunk's first L tokens (the chunk starts
+// at token t0).
+__device__ __forceinline__ void store_o(const Params &p, uint32_t tmem, uint32_t ocol, int lq, int cq, int lane,
+                                        int t0, int L, int h) {
     uint32_t r[32];
-    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + ocol + 32 * cq, r);
     const int row = 32 * (lq - 2) + lane;
     if (row < L) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + row) * p.H + h) * VD + 32 * cq);
@@ -444,15 +454,15 @@ __device__ __forceinline__ void store_o(const Params &p, uint32_t tmem, int lq, 
 }
 
 // O of a full chunk by tensor store: the warp stages its 32 tokens x 32
-// channels as one 64-byte-swizzled box (2 KB) in rows 0..63 of the [-W; Q~]
-// tile, free until the -W read-out, and lane 0 stores it; lane 0 waits for the
-// box to be read (tma_store_wait_read) before that tile is written again.
+// channels as one 64-byte-swizzled box (2 KB) in the staging tile, and lane 0
+// stores it; lane 0 waits for the box to be read (tma_store_wait_read) before
+// the staging tile is written again.
 __device__ __forceinline__ void store_o_tma(const Params &p, uint8_t *sm, uint32_t sbase, uint32_t tmem,
-                                            int lq, int cq, int lane, int t0, int h) {
+                                            uint32_t ocol, int lq, int cq, int lane, int t0, int h) {
     uint32_t r[32];
-    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+    KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + ocol + 32 * cq, r);
     const int box = 4 * (lq - 2) + cq;
-    const uint32_t stage = OP_A3 + (box >> 2) * 16384 + (box & 3) * 2048;
+    const uint32_t stage = OP_OST + box * 2048;
     const float sc = p.scale;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -546,7 +556,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     float *Rws = reinterpret_cast<float *>(sm + SCR_RW);   // per-warp R scratch of the solve
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     const uint32_t bar_qkg = sbase + SM_BAR, bar_v = sbase + SM_BAR + 8,
-                   bar_mma = sbase + SM_BAR + 16, bar_st = sbase + SM_BAR + 24;
+                   bar_mma = sbase + SM_BAR + 16, bar_st = sbase + SM_BAR + 24,
+                   bar_p = sbase + SM_BAR + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM_MISC);
     int *flags = reinterpret_cast<int *>(sm + SM_MISC + 4);
 
@@ -574,6 +585,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_st, 1);
+        mbar_init(bar_p, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *flags = 0;
         // the initial state, by four tensor copies into the staging tile
@@ -646,8 +658,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         beta_raw = __ldg(beta_bits + (size_t)(beta_ok ? bos + tid : bos) * p.H + h);
     }
     constexpr uint32_t ID_G1 = idesc(128, 64, 0, 0, 2);
-    constexpr uint32_t ID_G2 = idesc(128, 128, 0, 1, 1);
-    constexpr uint32_t ID_G3 = idesc(128, 128, 0, 1, 0);
+    constexpr uint32_t ID_P = idesc(128, 128, 0, 1, 0);
+    constexpr uint32_t ID_U = idesc(128, 128, 0, 1, 0);
     constexpr uint32_t ID_G4A = idesc(128, 128, 0, 1, 0);
     constexpr uint32_t ID_G4B = idesc(128, 128, 1, 1, 0);
     // This thread's share of the raw q, k, gk tiles, taken into registers while
@@ -686,7 +698,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     __syncthreads();   // the raw tiles may now be overwritten
     bool aborted = (*flags & FLAG_TIMEOUT) != 0;
     bool fb_prev = false;   // the previous chunk took the recurrent path (its o is written)
-    uint32_t nmma = 0;      // MMA commits waited for so far: the parity of the next
+    uint32_t nmma = 0;      // commits of bar_mma waited for so far: the parity of the next
+    uint32_t np = 0;        // P products issued so far (one commit of bar_p each)
     for (int c = 0; c < nchunks && !aborted; ++c) {
         const int t0 = bos + c * C;
         const int L = min(C, eos - t0);
@@ -761,7 +774,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 store_f32x8(sm, OP_A1, r, ch, 128, kf);
                 store_f32x8(sm, OP_A1, 64 + r, ch, 128, qr);
                 store_f32x8(sm, OP_B1, r, ch, 64, kb);
-                store_bf16(sm, OP_KT + chunk_off(r, ch, 64), kt);
+                store_f16(sm, OP_A3 + chunk_off(r, ch, 128), kt);
                 store_f16(sm, OP_KE + chunk_off(r, ch, 64), ke);
                 store_f16(sm, OP_A3 + chunk_off(64 + r, ch, 128), qt);
             }
@@ -780,8 +793,17 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         fb_next = false;
         bool raw_next = false, o_prev = false, v_next = false;
 
+        const uint32_t pcol = TM_P + 128u * par, pcol_prev = TM_P + 128u * (par ^ 1u);
+        const uint32_t ppar = np & 1u;   // parity of this chunk's P commit
+        const bool p_issued = !fb;
         if (!fb) {
-        // (3) G1 on TF32: [Kf; Qr] Kb^T, 16 steps of K = 8
+        ++np;
+        // (3) G1 on TF32: [Kf; Qr] Kb^T (16 steps of K = 8); then P = [K~; Q~] S0
+        //     (8 steps of K = 16) into this chunk's P columns.  P does not depend
+        //     on the triangular solve, so it runs while the Gram matrix is read
+        //     out and inverted.
+        // G1 and P come from two threads (each commit tracks its own thread's
+        // MMAs), so that thread 0 waits for G1 while P is still being issued.
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -789,6 +811,13 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 mma_tf32(tmem, sdesc(sbase + OP_A1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
                          sdesc(sbase + OP_B1 + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), ID_G1, s > 0);
             mma_commit(bar_mma);
+        } else if (tid == 32) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma(tmem + pcol, sdesc(sbase + OP_A3 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                    sdesc(sbase + OP_S + s * 2048, 16384, 1024), ID_P, s > 0);
+            mma_commit(bar_p);
         }
 
         // (4) A -> fp32 scratch (strictly lower, x beta_r); Aqk -> fp16 rows
@@ -823,8 +852,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = (16 * cq + j <= row) ? __uint_as_float(r[j]) : 0.f;
                 aqm = absmax(v, 16);
-                store_f16(sm, OP_TBZ + (uint32_t)(128 + row) * 128 + ((((2 * cq) ^ row) & 7) << 4), v);
-                store_f16(sm, OP_TBZ + (uint32_t)(128 + row) * 128 + ((((2 * cq + 1) ^ row) & 7) << 4),
+                store_f16(sm, OP_TBZ + (uint32_t)(64 + row) * 128 + ((((2 * cq) ^ row) & 7) << 4), v);
+                store_f16(sm, OP_TBZ + (uint32_t)(64 + row) * 128 + ((((2 * cq + 1) ^ row) & 7) << 4),
                           v + 8);
             }
         }
@@ -833,12 +862,50 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         }
         if (!fb) {
         // (5) T = (I + A)^-1 in 16 x 16 blocks: diagonal blocks T_II by forward
-        //     substitution (warps 0-1, one block per half-warp, lane = column),
-        //     then each warp completes its block column (solve_block_column).
-        //     Meanwhile the warps of TMEM lanes 64..127 write out the previous
-        //     chunk's O, which nothing overwrites before G2.
-        if (warp < 2) {
-            const int I = 2 * warp + (lane >> 4), col = lane & 15;
+        //     substitution (warps 2-3), then block columns (solve_block_column,
+        //     warps 0-5); T Diag(b) goes to TBZ in fp16.  During the diagonal
+        //     phase warps 6, 7, 10, 11, 14, 15 write out the previous chunk's O, and
+        //     the eight warps of sub-partitions 0 and 1 (TMEM lanes 0..63) read
+        //     K~ S0 out of P and turn v into V' = V - K~ S0 (fp16, in place), so
+        //     that the block columns run with nothing else beside them.
+        float xm = 0.f;   // magnitude of this thread's fp16 operands (T Diag(b) or V')
+        if (lq < 2) {
+            // sub-partitions 0 and 1 (TMEM lanes 0..63): zero the blocks of T Diag(b)
+            // above the diagonal, then V' = V - K~ S0 for token row 32 lq + lane,
+            // value channels 32 cq .. 32 cq + 31
+            const int t = 64 * cq + 32 * lq + lane;   // 0 .. 255
+            if (t < 96) {   // 6 upper blocks x 16 rows, two 16-byte chunks each
+                const int blk = t >> 4, r = t & 15;
+                const int I = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
+                const int J = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                const int rr = 16 * I + r;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int cchunk = 2 * J + h2;
+                    *reinterpret_cast<uint4 *>(sm + OP_TBZ + rr * 128 + (((cchunk ^ rr) & 7) << 4)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            const int row = 32 * lq + lane;
+            if (!barrier_wait_for(bar_p, ppar, wait_ns) || !barrier_wait_for(bar_v, par, wait_ns))
+                atomicOr(flags, FLAG_TIMEOUT);
+            tc_fence_after();
+            uint32_t r[32];
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + pcol + 32 * cq, r);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t off = RAW_V + chunk_off(row, 32 * cq + 8 * j, 64);
+                float vv[8];
+                unpack_bf16(*reinterpret_cast<const uint4 *>(sm + off), vv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vv[e] = row < L ? vv[e] - __uint_as_float(r[8 * j + e]) : 0.f;
+                xm = maxnan(xm, absmax(vv, 8));
+                store_f16(sm, off, vv);
+            }
+            tc_fence_before();
+        } else if (warp == 2 || warp == 3) {
+            // diagonal blocks: one block per half-warp, lane = column
+            const int I = 2 * (warp - 2) + (lane >> 4), col = lane & 15;
             const float *Ab = As + 16 * I * AS + 16 * I;   // diagonal block I, row stride AS
             // Column-oriented substitution: once x[j] is final, every later row
             // takes its term.  The chain is one FMA per step; rows load their
@@ -866,94 +933,53 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
             for (int r = 0; r < 16; ++r) {
                 const int rr = 16 * I + r;
                 Ts[rr * 64 + tsw(r, c)] = x[r];
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OP_TBZ + rr * 128 + ((((c >> 3) ^ rr) & 7) << 4) +
-                                                   (c & 7) * 2) = __float2bfloat16_rn(x[r] * bc);
+                const float tv = x[r] * bc;
+                xm = maxnan(xm, fabsf(tv));
+                *reinterpret_cast<__half *>(sm + OP_TBZ + rr * 128 + ((((c >> 3) ^ rr) & 7) << 4) +
+                                            (c & 7) * 2) = __float2half_rn(tv);
             }
-        } else if (lq >= 2 && c > 0 && !fb_prev) {
-            store_o_tma(p, sm, sbase, tmem, lq, cq, lane, t0 - C, h);
+        } else if (warp >= 6 && c > 0 && !fb_prev) {
+            // the previous chunk's O by tensor stores (32 x 32 boxes): warps 6 and 7
+            // take column quarters 0 and 1, warps 10, 11 quarter 2, warps 14, 15 quarter 3
+            const int q0 = warp < 8 ? 0 : (warp < 12 ? 2 : 3), nq = warp < 8 ? 2 : 1;
+#pragma unroll 1
+            for (int q = q0; q < q0 + nq; ++q) store_o_tma(p, sm, sbase, tmem, pcol_prev, lq, q, lane, t0 - C, h);
             tc_fence_before();
         }
         o_prev = true;
-        if (warp >= 4) {
-            // zero blocks above the diagonal of T Diag(b) and the zero rows 64..127
-            const int t = tid - 128;                   // 0 .. 383
-            *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * t) = make_uint4(0, 0, 0, 0);
-            if (t < 128) *reinterpret_cast<uint4 *>(sm + OP_TBZ + 8192 + 16 * (384 + t)) = make_uint4(0, 0, 0, 0);
-            if (t < 96) {   // 6 upper blocks x 16 rows, two 16-byte chunks each
-                const int blk = t >> 4, r = t & 15;
-                const int I = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
-                const int J = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                const int rr = 16 * I + r;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int cchunk = 2 * J + h2;
-                    *reinterpret_cast<uint4 *>(sm + OP_TBZ + rr * 128 + (((cchunk ^ rr) & 7) << 4)) =
-                        make_uint4(0, 0, 0, 0);
-                }
-            }
-        }
         __syncthreads();
-        if (warp < 2) solve_block_column<0>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
-        else if (warp < 4) solve_block_column<1>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
-        else if (warp < 6) solve_block_column<2>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1);
-        if (lq >= 2 && lane == 0 && c > 0 && !fb_prev) tma_store_wait_read();   // the O boxes before the -W read-out
+        // block columns J = 0, 1, 2 on warps (0, 1), (2, 3), (4, 5): one warp-level
+        // tensor unit per sub-partition and chain, as far as it goes
+        if (warp < 2) xm = maxnan(xm, solve_block_column<0>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1));
+        else if (warp < 4) xm = maxnan(xm, solve_block_column<1>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1));
+        else if (warp < 6) xm = maxnan(xm, solve_block_column<2>(As, Ts, Rws + warp * 16 * RW, lane, sm + OP_TBZ, beta_s, warp & 1));
+        if (warp >= 6 && lq >= 2 && lane == 0 && c > 0 && !fb_prev) tma_store_wait_read();   // the O boxes are read
         fence_proxy_async();
-        __syncthreads();
-
-        // (6) G2: [T Diag(b); 0] x [K~ | V]
+        fb = __syncthreads_or(!(xm <= FP16_LIMIT));
+        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
+        }
+        if (!fb) {
+        // (6) U = [T Diag(b); Aqk] V' (rows 0-63 kept)
         if (tid == 0) {
-            if (!barrier_wait_for(bar_v, par, wait_ns)) atomicOr(flags, FLAG_TIMEOUT);
             tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = sdesc(sbase + OP_TBZ + s * 32, 16, 1024);
-                mma(tmem, a, sdesc(sbase + OP_KT + s * 2048, 8192, 1024), ID_G2, s > 0);
-                mma(tmem + 128, a, sdesc(sbase + RAW_V + s * 2048, 8192, 1024), ID_G2, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma(tmem, sdesc(sbase + OP_TBZ + s * 32, 16, 1024), sdesc(sbase + RAW_V + s * 2048, 8192, 1024),
+                    ID_U, s > 0);
             mma_commit(bar_mma);
         }
         mma_wait_all(bar_mma, (nmma++) & 1u, flags, wait_ns);
-        // (7) -W -> fp16 rows 0..63 of [-W; Q~]; prefetch the next v (G2 consumed it)
+        // (7) U -> fp16 MN-major [token][v]; prefetch the next v (U consumed V')
         v_next = true;
-        float wm = 0.f;
         if (tid == 0 && c + 1 < nchunks) {
             mbar_expect_tx(bar_v, 16384);
             for (int b = 0; b < 2; ++b)
                 tma_load_3d(sbase + RAW_V + b * 8192, &p.tv, bar_v, 64 * b, h, t0 + C);
         }
-        if (lq < 2) {
-            uint32_t r[32];
-            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
-            const int row = 32 * lq + lane;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = -__uint_as_float(r[j]);
-            wm = absmax(v, 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                store_f16(sm, OP_A3 + chunk_off(row, 32 * cq + 8 * j, 128), v + 8 * j);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        fb = __syncthreads_or(!(wm <= FP16_LIMIT));
-        if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
-        }
-        if (!fb) {
-        // (8) G3: [-W; Q~] x S0 accumulated onto [U~; 0]
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma(tmem + 128, sdesc(sbase + OP_A3 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
-                    sdesc(sbase + OP_S + s * 2048, 16384, 1024), ID_G3, 1);
-            mma_commit(bar_mma);
-        }
-        mma_wait_all(bar_mma, (nmma++) & 1u, flags, wait_ns);
-        // (9) U -> fp16 MN-major [token][v]
         float um = 0.f;
         if (lq < 2) {
             uint32_t r[32];
-            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 128 + 32 * cq, r);
+            KDA_TMEM_LD32(tmem + ((uint32_t)(32 * lq) << 16) + 32 * cq, r);
             const int row = 32 * lq + lane;
             float v[32];
 #pragma unroll
@@ -968,13 +994,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         fb = __syncthreads_or(!(um <= FP16_LIMIT));
         }
         if (!fb) {
-        // (10) G4a: [0; Aqk] x U onto cols 128..; G4b: K_end^T x U into cols 0..127
+        // (8) G4a: [T Diag(b); Aqk] x U onto P (rows 64..127: Q~ S0 becomes O);
+        //     G4b: K_end^T x U into cols 0..127
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t b = sdesc(sbase + OP_U + s * 2048, 8192, 1024);
-                mma(tmem + 128, sdesc(sbase + OP_TBZ + 8192 + s * 32, 16, 1024), b, ID_G4A, 1);
+                mma(tmem + pcol, sdesc(sbase + OP_TBZ + s * 32, 16, 1024), b, ID_G4A, 1);
                 mma(tmem, sdesc(sbase + OP_KE + s * 2048, 8192, 1024), b, ID_G4B, s > 0);
             }
             mma_commit(bar_mma);
@@ -987,7 +1014,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         load_raw();
         mma_wait_all(bar_mma, (nmma++) & 1u, flags, wait_ns);
         if (*flags & FLAG_TIMEOUT) { aborted = true; break; }
-        // (11) the state update (O is written out during the next chunk's solve)
+        // (9) the state update (O is written out during the next chunk's solve)
         {
             // two 16-column reads keep the next chunk's raw tiles in registers
             const float gm = gam_s[(c & 1) * 128 + srow];
@@ -1006,11 +1033,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
         }
         // No block barrier here: each warp goes on to the next chunk's loads
         // and scan.  The next chunk's first barrier orders these TMEM reads
-        // before G1 overwrites the columns, and these S stores before G3 reads
+        // before G1 overwrites the columns, and these S stores before P reads
         // them (they reach the MMA's proxy through the fence below).  gam_s is
         // double-buffered by chunk parity; nothing else this epilogue reads is
-        // written before that barrier.  O stays in columns 128..255 until the
-        // next chunk's G2.
+        // written before that barrier.  O stays in this chunk's P columns until
+        // the next chunk's solve.
         fence_proxy_async();
         tc_fence_before();
         } else {
@@ -1033,10 +1060,13 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                     }
                 }
             }
+            // P, if issued, reads the tiles the staged state is written over
+            if (tid == 0 && p_issued && !barrier_wait_for(bar_p, ppar, wait_ns)) atomicOr(flags, FLAG_TIMEOUT);
             if (!o_prev && c > 0 && !fb_prev && lq >= 2) {   // the previous chunk's O, still in TMEM
                 tc_fence_after();
-                store_o(p, tmem, lq, cq, lane, t0 - C, C, h);
+                store_o(p, tmem, pcol_prev, lq, cq, lane, t0 - C, C, h);
             }
+            __syncthreads();
             float *P = reinterpret_cast<float *>(sm + STG);
 #pragma unroll
             for (int j = 0; j < 32; ++j) P[srow * FB_LD + 32 * cq + j] = S[j];
@@ -1063,7 +1093,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
     if (!aborted && nchunks > 0 && lq >= 2 && !fb_prev) {
         tc_fence_after();
         const int tl = bos + (nchunks - 1) * C;
-        store_o(p, tmem, lq, cq, lane, tl, eos - tl, h);
+        store_o(p, tmem, TM_P + 128u * ((nchunks - 1) & 1), lq, cq, lane, tl, eos - tl, h);
     }
 
     if (aborted) {
