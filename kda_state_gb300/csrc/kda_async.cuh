@@ -59,6 +59,13 @@ __device__ __forceinline__ void bulk_copy(void *dst_shared, const void *src_glob
         "l"(reinterpret_cast<uint64_t>(src_global)), "r"(bytes), "r"(bar)
         : "memory");
 }
+// Ask for bytes (a multiple of 16) of global memory to be brought into L2,
+// without waiting and without a destination in shared memory.
+__device__ __forceinline__ void prefetch_l2(const void *src_global, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src_global)),
+                 "r"(bytes)
+                 : "memory");
+}
 // Order this thread's earlier generic-proxy accesses of shared memory before
 // later async-proxy (bulk copy) writes to it.
 __device__ __forceinline__ void fence_async_shared() {

@@ -86,40 +86,33 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
 //     A[r][j]   = b_r <k_r E_r, k_j / E_j>   (j < r),   T = (I + A)^-1
 //     Aqk[r][j] = <q_r E_r, k_j / E_j>       (j <= r)
 //     W = T Diag(b) (K . E),  U~ = T Diag(b) V,  U = U~ - W h0
-//     O = (Q . E) h0 + Aqk U
-// The state is read once; the G x 128 x 128 products with h0 run on the CUDA
-// cores in fp32 (2G vectors against the register-resident h0).  A unit whose
-// decay over the draft leaves fp32 range for 1/E falls back to the recurrent
-// form.  Thread mapping for h0: warp w owns columns 16w .. 16w+15, lane l
-// column 16w + (l & 15) and rows 64 (l >> 4) .. + 63.
-constexpr int XS = KD + 4;   // padded row stride of W and q . E (conflict-free fragment loads)
-
-constexpr int HS = KD + 8;   // row stride of the staged h0: conflict-free B-fragment loads
-
-// H0S: h0 staged in shared memory by bulk copies (the tensor path), one row
-// of 512 bytes per copy into rows HS floats apart.
-template <int GM, bool H0S>
+//     O = (Q . E) h0 + Aqk U = M h0 + N,  M = Q . E - Aqk W,  N = Aqk U~
+// M and N depend on the draft alone, so h0 enters one G x 128 x 128 product
+// (fp32 FMAs) that streams h0 once, column by column, from L2: a bulk
+// prefetch asks for it when the unit starts, and nothing of h0 is staged in
+// shared memory.  A unit whose decay products over the draft leave
+// (1e-30, 1e30), where k / E stops being exact in fp32, takes the recurrence
+// instead (verify_unit_sliced).
+template <int GM>
 struct VerifyBlockSmem {
-    float kg[GM][KD];   // k . E
-    float kn[GM][KD];   // k / E
-    float qg[GM][XS];   // q . E
-    float v[GM][VD];
-    float w[GM][XS];    // W
-    float ut[GM][VD];   // U~
+    float kg[GM][KD];   // k . E; in the recurrent path alpha = exp(gk)
+    float kn[GM][KD];   // k / E; in the recurrent path k
+    float qg[GM][KD];   // q . E, then M = Q . E - Aqk W; in the recurrent path q
+    float v[GM][VD];    // v, then half of M h0 (rows 0..63)
     float akk[GM][GM], aqk[GM][GM], tb[GM][GM];
     float beta[GM];
+    float kq[GM];       // recurrent path: k . q per token
+    float red[2][8][32];   // recurrent path: partial sums of S'^T k and S'^T q
+    float u[32];
     int fallback;
-    int h0_ok;
-    alignas(8) uint64_t bar;
-    alignas(16) float h0s[H0S ? KD : 1][HS];
 };
 
 // ---------------------------------------------------------------------------
 // Block-form phases of one unit.  Each is followed by a block barrier in the
 // caller.
 // ---------------------------------------------------------------------------
-template <int GM, bool H0S>
-__device__ __forceinline__ void block_gram(VerifyBlockSmem<GM, H0S> &sm, int G, int warp, int lane) {
+template <int GM>
+__device__ __forceinline__ void block_gram(VerifyBlockSmem<GM> &sm, int G, int warp, int lane) {
     // Gram rows: warp w takes draft rows r = w, w + 8, ...; each lane holds 4
     // channels of k_r E_r and q_r E_r and accumulates the row's products with
     // every k_j / E_j, then one butterfly per product (independent, so they
@@ -139,27 +132,42 @@ __device__ __forceinline__ void block_gram(VerifyBlockSmem<GM, H0S> &sm, int G, 
                 dq[j] = qr4.x * y.x + qr4.y * y.y + qr4.z * y.z + qr4.w * y.w;
             }
         }
+        // Reduce the 2 GM partial sums across the warp by halving: at each step a
+        // lane keeps half of its values and adds its partner's copy of that half,
+        // so the steps move GM, GM / 2, ... values instead of all 2 GM each time.
+        // Afterwards lane l holds the total of value (l >> s) (s = 1 for GM = 8,
+        // 0 for GM = 16): values 0 .. GM-1 are dk, GM .. 2GM-1 are dq.
+        float v[2 * GM];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
+        for (int j = 0; j < GM; ++j) {
+            v[j] = dk[j];
+            v[GM + j] = dq[j];
+        }
 #pragma unroll
-            for (int j = 0; j < GM; ++j) {
-                dk[j] += __shfl_xor_sync(0xffffffffu, dk[j], off);
-                dq[j] += __shfl_xor_sync(0xffffffffu, dq[j], off);
+        for (int n = 2 * GM, off = 16; n > 1; n >>= 1, off >>= 1) {
+            const bool hi = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = hi ? v[i] : v[i + n / 2];
+                const float keep = hi ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
             }
         }
-        if (lane == 0) {
-            const float br = sm.beta[r];
-#pragma unroll
-            for (int j = 0; j < GM; ++j) {
-                if (j < r) sm.akk[r][j] = dk[j] * br;
-                if (j <= r) sm.aqk[r][j] = dq[j];
+        constexpr int SH = GM == 8 ? 1 : 0;
+        if (SH) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        const int idx = lane >> SH;
+        if ((lane & ((1 << SH) - 1)) == 0) {
+            if (idx < GM) {
+                if (idx < r) sm.akk[r][idx] = v[0] * sm.beta[r];
+            } else if (idx - GM <= r) {
+                sm.aqk[r][idx - GM] = v[0];
             }
         }
     }
 }
 
-template <int GM, bool H0S>
-__device__ __forceinline__ void block_solve(VerifyBlockSmem<GM, H0S> &sm, int G, int warp, int lane) {
+template <int GM>
+__device__ __forceinline__ void block_solve(VerifyBlockSmem<GM> &sm, int G, int warp, int lane) {
     // T = (I + A)^-1 by forward substitution (lane = column), then T Diag(b).
     // Each row's entries of A are loaded before its FMA chain (they do not
     // depend on x), so the loads overlap the previous rows' chains.
@@ -186,77 +194,72 @@ __device__ __forceinline__ void block_solve(VerifyBlockSmem<GM, H0S> &sm, int G,
     }
 }
 
-template <int GM, bool H0S>
-__device__ __forceinline__ void block_wu(VerifyBlockSmem<GM, H0S> &sm, int G, int tid) {
-    // W = T Diag(b) (K . E) and U~ = T Diag(b) V, one column per thread
-    const int c = tid & (KD - 1);
-    const bool do_w = tid < KD;
-    for (int r = 0; r < GM; ++r) {
-        float acc = 0.f;
-        if (r < G)
-            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], do_w ? sm.kg[j][c] : sm.v[j][c], acc);
-        if (do_w) {
-            sm.w[r][c] = acc;
-            if (r >= G) sm.qg[r][c] = 0.f;
-        } else {
-            sm.ut[r][c] = acc;
+// The recurrence over the draft, one 32-column slice of the state at a time
+// (the update separates by value column): thread t holds rows 16 (t / 32) ..
+// + 15 of column 32 slice + (t % 32).  Its token inputs (alpha, k, q, v, beta,
+// k . q) are staged first; o of every token is stored.  Used when the block
+// form's k / E would leave fp32's exact range.
+template <typename T, int GM>
+__device__ __noinline__ void verify_unit_sliced(const VerifyArgs &a, VerifyBlockSmem<GM> &sm, const float *S0,
+                                                size_t tok0, int G, int h) {
+    const int t = threadIdx.x, cl = t & 31, rg = t >> 5;
+    if (t < KD) {
+        for (int i = 0; i < G; ++i) {
+            const size_t tok = (tok0 + i) * a.H + h;
+            const float kk = to_f(((const T *)a.k)[tok * KD + t]);
+            const float qq = to_f(((const T *)a.q)[tok * KD + t]);
+            sm.kg[i][t] = expf(to_f(((const T *)a.gk)[tok * KD + t]));
+            sm.kn[i][t] = kk;
+            sm.qg[i][t] = qq;
+            float d = kk * qq;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            if ((t & 31) == 0) sm.red[0][t >> 5][i] = d;   // k . q, 4 warps' parts
         }
     }
-}
-
-// [W; Q . E] h0 on warp-level TF32 MMAs with h0 from shared memory, then
-// U = U~ - W h0 and O = (Q . E) h0 + Aqk U; writes the G output rows.
-template <typename T>
-__device__ __forceinline__ void block_tensor_out(VerifyBlockSmem<8, true> &sm, const VerifyArgs &a,
-                                                 size_t tok0, int G, int h, int warp, int lane) {
-    constexpr int GM = 8;
-    const int g = lane >> 2, t4 = lane & 3;
-    // [W; Q . E] (16 x 128) h0 (128 x 16 columns of this warp): 16 k-steps x
-    // 2 n-tiles of m16n8k8 TF32.  Row g of the result is W row g (c[.][0..1])
-    // and (Q . E) row g (c[.][2..3]) at columns 16w + 8nt + 2t4 (+1).
-    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    __syncthreads();
+    if (t < GM && t < G) sm.kq[t] = (sm.red[0][0][t] + sm.red[0][1][t]) + (sm.red[0][2][t] + sm.red[0][3][t]);
+    __syncthreads();
+    for (int sl = 0; sl < VD / 32; ++sl) {
+        const int col = 32 * sl + cl;
+        float s[16];
 #pragma unroll
-    for (int ks = 0; ks < 16; ++ks) {
-        const int k = 8 * ks + t4;
-        const uint32_t af[4] = {tf32_bits(sm.w[g][k]), tf32_bits(sm.qg[g][k]),
-                                tf32_bits(sm.w[g][k + 4]), tf32_bits(sm.qg[g][k + 4])};
+        for (int j = 0; j < 16; ++j) s[j] = S0[(size_t)(16 * rg + j) * VD + col];
+        for (int i = 0; i < G; ++i) {
+            float pw = 0.f, pq = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const float *hb = &sm.h0s[8 * ks + t4][16 * warp + 8 * nt + g];
-            const uint32_t bf[2] = {tf32_bits(hb[0]), tf32_bits(hb[4 * HS])};
-            mma16n8k8_tf32(c[nt], af, bf);
-        }
-    }
-    // U = U~ - W h0 for row g; O = (Q . E) h0 + Aqk U, U rows from the lanes
-    // holding them (lane 4j + t4)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int c0 = 16 * warp + 8 * nt + 2 * t4;
-        const float u0 = sm.ut[g][c0] - c[nt][0], u1 = sm.ut[g][c0 + 1] - c[nt][1];
-        float o0 = c[nt][2], o1 = c[nt][3];
-#pragma unroll
-        for (int j = 0; j < GM; ++j) {
-            const float uj0 = __shfl_sync(0xffffffffu, u0, 4 * j + t4);
-            const float uj1 = __shfl_sync(0xffffffffu, u1, 4 * j + t4);
-            if (j <= g && j < G) {
-                const float aq = sm.aqk[g][j];
-                o0 = fmaf(aq, uj0, o0);
-                o1 = fmaf(aq, uj1, o1);
+            for (int j = 0; j < 16; ++j) {
+                const int kr = 16 * rg + j;
+                s[j] *= sm.kg[i][kr];
+                pw = fmaf(s[j], sm.kn[i][kr], pw);
+                pq = fmaf(s[j], sm.qg[i][kr], pq);
             }
-        }
-        if (g < G) {
-            T *dst = (T *)a.o + ((tok0 + g) * a.H + h) * VD + c0;
-            dst[0] = from_f<T>(a.scale * o0);
-            dst[1] = from_f<T>(a.scale * o1);
+            sm.red[0][rg][cl] = pw;
+            sm.red[1][rg][cl] = pq;
+            __syncthreads();
+            if (rg == 0) {
+                float w = 0.f, ps = 0.f;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    w += sm.red[0][g][cl];
+                    ps += sm.red[1][g][cl];
+                }
+                const float u = sm.beta[i] * (sm.v[i][col] - w);
+                sm.u[cl] = u;
+                ((T *)a.o)[((tok0 + i) * a.H + h) * VD + col] = from_f<T>(a.scale * (ps + u * sm.kq[i]));
+            }
+            __syncthreads();
+            const float u = sm.u[cl];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s[j] = fmaf(sm.kn[i][16 * rg + j], u, s[j]);
         }
     }
 }
 
 template <typename T, int GM>
-__global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
-    VerifyBlockSmem<GM, TENSOR> &sm = *reinterpret_cast<VerifyBlockSmem<GM, TENSOR> *>(smem);
+    VerifyBlockSmem<GM> &sm = *reinterpret_cast<VerifyBlockSmem<GM> *>(smem);
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit - b * a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -272,26 +275,13 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         return;
     }
     if (G == 0) return;
-    // h0 (read-only).  Tensor path (bf16 inputs, G <= 8): 128 bulk copies, one
-    // row each, land it in shared memory while the draft is staged and its
-    // matrices formed; the m16n8k8 B fragments are read from there.  CUDA-core
-    // path: registers, column 16w + (lane & 15), rows 64 (lane >> 4) .. + 63.
+    // h0 (read-only): into L2 now, read once by the final product
     const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS;
-    const int col = 16 * warp + (lane & 15), hr = lane >> 4;
-    float s[TENSOR ? 1 : 64];
-    const uint32_t bar = shared_addr(&sm.bar);
     if (tid == 0) {
         sm.fallback = 0;   // set by the staging below, after the barrier
-        if (TENSOR) {
-            barrier_init(bar, 1);
-            barrier_expect(bar, (uint32_t)(sizeof(float) * STATE_ELEMS));
-        }
+        prefetch_l2(S0, STATE_ELEMS * sizeof(float));
     }
-    if (!TENSOR) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __ldg(S0 + (size_t)(64 * hr + i) * VD + col);
-    }
-    __syncthreads();   // the reset, and the barrier the h0 copies (issued after the draft's loads) complete on
+    __syncthreads();
     const int base = a.ring_base ? a.ring_base[b] : 0;
     const int mask = a.ring_len - 1;
     // stage the draft, store the records; running decay products per channel.
@@ -308,9 +298,6 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                 gr[i] = ((const T *)a.gk)[tok * KD + c];
             }
         }
-        // h0 streams in behind the draft (8 KB), which the Gram, the solve and
-        // W / U~ need first; only the final product waits for h0
-        if (TENSOR) bulk_copy(sm.h0s[c], S0 + (size_t)c * VD, VD * sizeof(float), bar);
         float E = 1.f;
         bool tiny = false;
 #pragma unroll
@@ -321,7 +308,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
                 ((T *)a.rk)[e * KD + c] = kr[i];
                 a.rdecay[e * KD + c] = alpha;
                 E *= alpha;
-                tiny |= !(E > 1e-30f && E < 1e30f);   // outside: the recurrent fallback
+                tiny |= !(E > 1e-30f && E < 1e30f);   // outside: the recurrent path
                 const float kk = to_f(kr[i]), qq = to_f(qr[i]);
                 sm.kg[i][c] = kk * E;
                 sm.kn[i][c] = __fdividef(kk, E);   // used only for E in (1e-30, 1e30): within 2 ulp
@@ -355,70 +342,90 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
         }
     }
     __syncthreads();
-    if (sm.fallback) {
-        // The records above are the same ones the recurrent form stores; it
-        // rewrites them identically.  Its scratch reuses this shared memory,
-        // so the h0 copies must have landed first.
-        if (TENSOR && tid == 0) sm.h0_ok = barrier_wait(bar, 0);
-        __syncthreads();
-        if (TENSOR && !sm.h0_ok) {
-            if (tid == 0) report(a.err, DEVERR_TIMEOUT);
-            return;
-        }
-        verify_unit_recurrent<T>(a, b, h, slot, tok0, G, smem);
+    if (sm.fallback) {   // uniform: read after the barrier
+        verify_unit_sliced<T, GM>(a, sm, S0, tok0, G, h);
         return;
     }
     block_gram(sm, G, warp, lane);
     __syncthreads();
     block_solve(sm, G, warp, lane);
     __syncthreads();
-    block_wu(sm, G, tid);
-    if (TENSOR && tid == 0) sm.h0_ok = barrier_wait(bar, 0);   // h0 has landed
-    __syncthreads();
-    if constexpr (TENSOR) {
-        if (!sm.h0_ok) {
-            if (tid == 0) report(a.err, DEVERR_TIMEOUT);
-            return;
+    // W and M = Q . E - Aqk W (threads 0..127, column c, M in place of Q . E);
+    // U~ and N = Aqk U~ (threads 128..255, column c, N kept in registers)
+    const int c = tid & (KD - 1);
+    float n[GM];
+    if (tid < KD) {
+        float w[GM];
+#pragma unroll
+        for (int r = 0; r < GM; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], sm.kg[j][c], acc);
+            w[r] = r < G ? acc : 0.f;
         }
-        block_tensor_out<T>(sm, a, tok0, G, h, warp, lane);
+#pragma unroll
+        for (int r = 0; r < GM; ++r) {
+            float m = r < G ? sm.qg[r][c] : 0.f;
+#pragma unroll
+            for (int j = 0; j <= r; ++j) m = fmaf(-sm.aqk[r][j], w[j], m);
+            sm.qg[r][c] = r < G ? m : 0.f;
+        }
     } else {
-        // [W; Q . E] h0 for this thread's column: partial over its 64 rows, then
-        // the other row half via one shuffle.  acc[i] (i < GM) is row i of W,
-        // acc[GM + i] row i of Q . E.
-        float acc[2 * GM];
+        float ut[GM];
 #pragma unroll
-        for (int i = 0; i < 2 * GM; ++i) acc[i] = 0.f;
+        for (int r = 0; r < GM; ++r) {
+            float acc = 0.f;
 #pragma unroll
-        for (int k4 = 0; k4 < 16; ++k4) {
-            const int k = 64 * hr + 4 * k4;
+            for (int j = 0; j <= r; ++j) acc = fmaf(sm.tb[r][j], sm.v[j][c], acc);
+            ut[r] = r < G ? acc : 0.f;
+        }
 #pragma unroll
-            for (int i = 0; i < 2 * GM; ++i) {
-                if ((i < GM ? i : i - GM) < G) {
-                    const float *row = (i < GM) ? sm.w[i] : sm.qg[i - GM];
-                    const float4 x = *reinterpret_cast<const float4 *>(row + k);
-                    acc[i] = fmaf(x.x, s[4 * k4], acc[i]);
-                    acc[i] = fmaf(x.y, s[4 * k4 + 1], acc[i]);
-                    acc[i] = fmaf(x.z, s[4 * k4 + 2], acc[i]);
-                    acc[i] = fmaf(x.w, s[4 * k4 + 3], acc[i]);
+        for (int r = 0; r < GM; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j <= r; ++j) acc = fmaf(sm.aqk[r][j], ut[j], acc);
+            n[r] = acc;
+        }
+    }
+    __syncthreads();
+    // M h0: thread (column c, half hf) sums over rows 64 hf .. 64 hf + 63 of h0,
+    // 16 rows' loads in flight at a time; each warp load is one 128-byte piece
+    // of a row.  Rows of M past G are zero.
+    const int hf = tid >> 7;
+    float acc[GM];
+#pragma unroll
+    for (int r = 0; r < GM; ++r) acc[r] = 0.f;
+    const float *hp = S0 + (size_t)(64 * hf) * VD + c;
+#pragma unroll 1
+    for (int k16 = 0; k16 < 4; ++k16) {
+        float hv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hv[e] = __ldcs(hp + (size_t)(16 * k16 + e) * VD);
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const int kk = 64 * hf + 16 * k16 + 4 * e4;
+#pragma unroll
+            for (int r = 0; r < GM; ++r) {
+                if (r < G) {
+                    const float4 m = *reinterpret_cast<const float4 *>(&sm.qg[r][kk]);
+                    acc[r] = fmaf(m.x, hv[4 * e4], acc[r]);
+                    acc[r] = fmaf(m.y, hv[4 * e4 + 1], acc[r]);
+                    acc[r] = fmaf(m.z, hv[4 * e4 + 2], acc[r]);
+                    acc[r] = fmaf(m.w, hv[4 * e4 + 3], acc[r]);
                 }
             }
         }
+    }
+    if (hf == 0) {
 #pragma unroll
-        for (int i = 0; i < 2 * GM; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
-        // U = U~ - W h0;  O = (Q . E) h0 + Aqk U;  each row half writes half the rows
-        float u[GM];
+        for (int r = 0; r < GM; ++r) sm.v[r][c] = acc[r];
+    }
+    __syncthreads();
+    if (hf == 1) {
 #pragma unroll
-        for (int r = 0; r < GM; ++r) u[r] = (r < G) ? sm.ut[r][col] - acc[r] : 0.f;
-        const int half = (G + 1) / 2;
-#pragma unroll
-        for (int r = 0; r < GM; ++r) {
-            if (r < G && ((r < half) == (hr == 0))) {
-                float o = acc[GM + r];
-#pragma unroll
-                for (int j = 0; j <= r; ++j) o = fmaf(sm.aqk[r][j], u[j], o);
-                ((T *)a.o)[((tok0 + r) * a.H + h) * VD + col] = from_f<T>(a.scale * o);
-            }
-        }
+        for (int r = 0; r < GM; ++r)
+            if (r < G)
+                ((T *)a.o)[((tok0 + r) * a.H + h) * VD + c] = from_f<T>(a.scale * ((sm.v[r][c] + acc[r]) + n[r]));
     }
 }
 
@@ -427,18 +434,13 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_block_kernel(VerifyArgs
 template <typename T, int GM>
 cudaError_t launch_verify_block(const VerifyArgs &a, cudaStream_t s) {
     const unsigned grid = (unsigned)a.B * (unsigned)a.H;
-    const size_t rec = sizeof(Reduce) + (size_t)a.G * sizeof(TokenIn);   // fallback's needs
-    constexpr bool TENSOR = (sizeof(T) == 2) && (GM == 8);
-    const size_t blk = sizeof(VerifyBlockSmem<GM, TENSOR>);
-    const size_t smem = blk > rec ? blk : rec;
+    const size_t smem = sizeof(VerifyBlockSmem<GM>);
     cudaError_t e = set_smem(verify_block_kernel<T, GM>, smem);
     if (e != cudaSuccess) return e;
     verify_block_kernel<T, GM><<<grid, CTA_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-// The recurrent fallback's scratch (Reduce + G TokenIn) must stay below h0s,
-// where copies may be in flight.
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s) {
     const bool bf = a.dt == KDA_DTYPE_BF16;
     if (a.G <= 8)
