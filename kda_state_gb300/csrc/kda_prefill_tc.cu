@@ -60,6 +60,7 @@
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <type_traits>
 #include <vector>
 
 #include "kda_async.cuh"
@@ -715,16 +716,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 
         // (2) cumulative decays and the operand tiles
         bool bad;
-        {
+        // FULL: all 64 rows are tokens of the sequence (no row masks)
+        auto prep = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
             const int ch = 8 * warp, sw = (lane >> 2) & 1;
             const int rA = 2 * lane + sw, rB = 2 * lane + 1 - sw;
             float gA[8], gB[8];
             unpack_bf16(wgA, gA);
             unpack_bf16(wgB, gB);
-            const bool vA = rA < L, vB = rB < L;
+            const bool vA = FULL || rA < L, vB = FULL || rB < L;
             // G at rows 2l and 2l+1: inclusive warp scan of the row-pair sums
             float gref[8], glast[8];
-            float gmax = 0.f, dmax = 0.f, qkmax = 0.f;
+            float gmax = 0.f, qkmax = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float a = vA ? gA[i] : 0.f, b = vB ? gB[i] : 0.f;
@@ -741,10 +744,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 gref[i] = __shfl_sync(0xffffffffu, s2, 15);    // G at row 31
                 glast[i] = __shfl_sync(0xffffffffu, s2, 31);   // G at row 63 (= last valid row)
             }
-            float egr[8], elr[8];   // per channel: exp(G_ref), exp(G_L - G_ref)
+            // With every gk <= 0 (checked: gmax) G never increases down the rows,
+            // and a sum of non-positive terms never increases under rounding
+            // either, so |G_r - G_ref| is largest at the first or the last row:
+            // at most -G_ref (the first row's G is <= 0) or G_ref - G_L.  A
+            // one-nat margin covers the rounding of the scan; NaN fails the check.
+            float egr[8], elr[8], gr2[8];   // per channel: exp(G_ref), exp(G_L - G_ref), G_ref log2(e)
+            float dmax = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                egr[i] = ex2(gref[i] * LOG2E);
+                dmax = maxnan3(dmax, -gref[i], gref[i] - glast[i]);
+                gr2[i] = gref[i] * LOG2E;
+                egr[i] = ex2(gr2[i]);
                 elr[i] = ex2((glast[i] - gref[i]) * LOG2E);
             }
 #pragma unroll
@@ -759,17 +770,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float q_ = valid ? qq[i] : 0.f, k_ = valid ? kk[i] : 0.f;
-                    const float d = (g[i] - gref[i]) * LOG2E;
+                    const float d = fmaf(g[i], LOG2E, -gr2[i]);   // (G_r - G_ref) log2(e)
                     qkmax = maxnan3(qkmax, fabsf(q_), fabsf(k_));
-                    dmax = maxnan(dmax, fabsf(d));
                     const float ef = ex2(d);                 // exp(G_r - G_ref)
                     const float eb = ex2(-d);                // exp(G_ref - G_r)
                     kf[i] = k_ * ef;
                     kb[i] = k_ * eb;
-                    kt[i] = k_ * (egr[i] * ef);              // k exp(G_r)
-                    ke[i] = k_ * (elr[i] * eb);              // k exp(G_L - G_r)
                     qr[i] = q_ * ef;
-                    qt[i] = q_ * (egr[i] * ef);              // q exp(G_r)
+                    kt[i] = kf[i] * egr[i];                  // k exp(G_r)
+                    qt[i] = qr[i] * egr[i];                  // q exp(G_r)
+                    ke[i] = kb[i] * elr[i];                  // k exp(G_L - G_r)
                 }
                 store_f32x8(sm, OP_A1, r, ch, 128, kf);
                 store_f32x8(sm, OP_A1, 64 + r, ch, 128, qr);
@@ -778,12 +788,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc_kernel(const __grid_constant
                 store_f16(sm, OP_KE + chunk_off(r, ch, 64), ke);
                 store_f16(sm, OP_A3 + chunk_off(64 + r, ch, 128), qt);
             }
-            bad = !(dmax <= D_LIMIT * LOG2E) || !(qkmax <= QK_LIMIT) || !(gmax <= 0.f);
+            bad = !(dmax <= D_LIMIT - 1.f) || !(qkmax <= QK_LIMIT) || !(gmax <= 0.f);
             if (lane == 31) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) gam_s[(c & 1) * 128 + ch + i] = expf(glast[i]);
             }
-        }
+        };
+        if (L == C) prep(std::integral_constant<bool, true>());
+        else prep(std::integral_constant<bool, false>());
         fence_proxy_async();
         // Every check of a chunk is decided before its state update; a chunk
         // outside the operand formats leaves the tensor-core path for the
