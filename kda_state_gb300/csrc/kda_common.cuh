@@ -132,8 +132,9 @@ __device__ __forceinline__ void state_store(const StateRegs &r, float *__restric
 
 // Stage one token's inputs (threads 0..127 each take one channel).  If rec_*
 // pointers are given, the step's record for the ReplaySSM ring is written too:
-// k and v as given, exp(gk) and beta as fp32.
-template <typename T, bool NEED_Q>
+// k and v as given, exp(gk) and beta as fp32.  Without ALPHA the caller has
+// staged in.alpha itself (gk is not read).
+template <typename T, bool NEED_Q, bool ALPHA = true>
 __device__ __forceinline__ void stage_token(TokenIn &in, const T *__restrict__ q,
                                             const T *__restrict__ k, const T *__restrict__ v,
                                             const T *__restrict__ gk, const T *__restrict__ beta,
@@ -144,14 +145,16 @@ __device__ __forceinline__ void stage_token(TokenIn &in, const T *__restrict__ q
     if (t < KD) {
         const T kr = k[t], vr = v[t];
         const float kk = to_f(kr);
-        const float a = expf(to_f(gk[t]));
         in.k[t] = kk;
-        in.alpha[t] = a;
         in.v[t] = to_f(vr);
+        if (ALPHA) {
+            const float a = expf(to_f(gk[t]));
+            in.alpha[t] = a;
+            if (rec_k) rec_decay[t] = a;
+        }
         if (rec_k) {
             rec_k[t] = kr;
             rec_v[t] = vr;
-            rec_decay[t] = a;
         }
         if (NEED_Q) {
             const float qq = to_f(q[t]);
