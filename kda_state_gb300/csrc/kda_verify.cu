@@ -18,6 +18,11 @@ namespace {
 // cu_drafts; the uniform call is the case cu_drafts[b] = b G.
 // ---------------------------------------------------------------------------
 
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 // Request b's first token and draft count; false (and an error bit) when the
 // ragged offsets are inconsistent.
 __device__ __forceinline__ bool draft_span(const VerifyArgs &a, int b, size_t &tok0, int &G) {
@@ -88,17 +93,20 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
 //     W = T Diag(b) (K . E),  U~ = T Diag(b) V,  U = U~ - W h0
 //     O = (Q . E) h0 + Aqk U = M h0 + N,  M = Q . E - Aqk W,  N = Aqk U~
 // M and N depend on the draft alone, so h0 enters one G x 128 x 128 product
-// (fp32 FMAs) that streams h0 once, column by column, from L2: a bulk
-// prefetch asks for it when the unit starts, and nothing of h0 is staged in
-// shared memory.  A unit whose decay products over the draft leave
+// that streams h0 once from L2: a bulk prefetch asks for it when the unit
+// starts, and nothing of h0 is staged in shared memory.  For bf16 inputs the
+// product runs as warp-level TF32 MMAs (operands rounded to nearest; about
+// 1e-3 of RMS on o, within the bf16 output's bound), for fp32 inputs as fp32
+// FMAs.  A unit whose decay products over the draft leave
 // (1e-30, 1e30), where k / E stops being exact in fp32, takes the recurrence
 // instead (verify_unit_sliced).
 template <int GM>
 struct VerifyBlockSmem {
     float kg[GM][KD];   // k . E; in the recurrent path alpha = exp(gk)
-    float kn[GM][KD];   // k / E; in the recurrent path k
-    float qg[GM][KD];   // q . E, then M = Q . E - Aqk W; in the recurrent path q
-    float v[GM][VD];    // v, then half of M h0 (rows 0..63)
+    float kn[GM][KD];   // k / E, then N (bf16 inputs); in the recurrent path k
+    float qg[GM][KD + 4];   // q . E, then M = Q . E - Aqk W; in the recurrent path q
+                            // (rows padded: the MMA product's fragment loads are conflict-free)
+    float v[GM][VD];    // v, then the k-half 0 partial of M h0
     float akk[GM][GM], aqk[GM][GM], tb[GM][GM];
     float beta[GM];
     float kq[GM];       // recurrent path: k . q per token
@@ -256,6 +264,132 @@ __device__ __noinline__ void verify_unit_sliced(const VerifyArgs &a, VerifyBlock
     }
 }
 
+// o = scale (M h0 + N) on fp32 FMAs (fp32 inputs): thread (column c, half hf)
+// sums over rows 64 hf .. 64 hf + 63 of h0, 16 rows' loads in flight at a
+// time; each warp load is one 128-byte piece of a row.  Rows of M past G are
+// zero.  N is in registers of threads 128..255 (column c).
+template <typename T, int GM>
+__device__ __forceinline__ void verify_product_fma(const VerifyArgs &a, VerifyBlockSmem<GM> &sm, const float *S0,
+                                                   size_t tok0, int G, int h, const float (&n)[GM]) {
+    const int tid = threadIdx.x, c = tid & (KD - 1), hf = tid >> 7;
+    float acc[GM];
+#pragma unroll
+    for (int r = 0; r < GM; ++r) acc[r] = 0.f;
+    const float *hp = S0 + (size_t)(64 * hf) * VD + c;
+#pragma unroll 1
+    for (int k16 = 0; k16 < 4; ++k16) {
+        float hv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hv[e] = __ldcs(hp + (size_t)(16 * k16 + e) * VD);
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const int kk = 64 * hf + 16 * k16 + 4 * e4;
+#pragma unroll
+            for (int r = 0; r < GM; ++r) {
+                if (r < G) {
+                    const float4 m = *reinterpret_cast<const float4 *>(&sm.qg[r][kk]);
+                    acc[r] = fmaf(m.x, hv[4 * e4], acc[r]);
+                    acc[r] = fmaf(m.y, hv[4 * e4 + 1], acc[r]);
+                    acc[r] = fmaf(m.z, hv[4 * e4 + 2], acc[r]);
+                    acc[r] = fmaf(m.w, hv[4 * e4 + 3], acc[r]);
+                }
+            }
+        }
+    }
+    if (hf == 0) {
+#pragma unroll
+        for (int r = 0; r < GM; ++r) sm.v[r][c] = acc[r];
+    }
+    __syncthreads();
+    if (hf == 1) {
+#pragma unroll
+        for (int r = 0; r < GM; ++r)
+            if (r < G)
+                ((T *)a.o)[((tok0 + r) * a.H + h) * VD + c] = from_f<T>(a.scale * ((sm.v[r][c] + acc[r]) + n[r]));
+    }
+}
+
+// o = scale (M h0 + N) as warp-level TF32 MMAs (bf16 inputs).  Warp w covers
+// value columns 32 (w & 3) .. + 31 over key rows 64 (w >> 2) .. + 63, in eight
+// k-steps of m16n8k8 (M's rows 0..15 as the A operand, rows past G zero).  The
+// warp's 32 columns form four n-tiles whose column n of tile j is value column
+// 4 n + j of the group, so lane (g, t4) takes its B operands of all four tiles
+// for key row k from one 16-byte load of h0[k][4 g .. 4 g + 3] (each warp load
+// reads four whole 128-byte row pieces), and its results for draft row g are
+// the group's value columns 8 t4 .. 8 t4 + 7.  The k-half 0 warps leave their
+// partial sums in sm.v; the k-half 1 warps add them and N (sm.kn) and store o.
+template <typename T, int GM>
+__device__ __forceinline__ void verify_product_mma(const VerifyArgs &a, VerifyBlockSmem<GM> &sm, const float *S0,
+                                                   size_t tok0, int G, int h, int warp, int lane) {
+    static_assert(GM == 8 || GM == 16, "draft rows fill one or two 8-row halves of the A operand");
+    const int cg = warp & 3, kh = warp >> 2, g = lane >> 2, t4 = lane & 3;
+    const int c0 = 32 * cg;
+    float d[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+    const float *hp = S0 + (size_t)(64 * kh + t4) * VD + c0 + 4 * g;
+#pragma unroll 1
+    for (int s2 = 0; s2 < 4; ++s2) {   // two k-steps per batch: four 16-byte loads in flight
+        float4 hb[2][2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            hb[s][0] = __ldcs(reinterpret_cast<const float4 *>(hp + (size_t)(16 * s2 + 8 * s) * VD));
+            hb[s][1] = __ldcs(reinterpret_cast<const float4 *>(hp + (size_t)(16 * s2 + 8 * s + 4) * VD));
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int k0 = 64 * kh + 16 * s2 + 8 * s;
+            uint32_t af[4];
+            af[0] = tf32_bits(sm.qg[g][k0 + t4]);
+            af[2] = tf32_bits(sm.qg[g][k0 + t4 + 4]);
+            af[1] = GM == 16 ? tf32_bits(sm.qg[(g + 8) % GM][k0 + t4]) : 0u;
+            af[3] = GM == 16 ? tf32_bits(sm.qg[(g + 8) % GM][k0 + t4 + 4]) : 0u;
+            const float lo[4] = {hb[s][0].x, hb[s][0].y, hb[s][0].z, hb[s][0].w};
+            const float hi[4] = {hb[s][1].x, hb[s][1].y, hb[s][1].z, hb[s][1].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t bf[2] = {tf32_bits(lo[j]), tf32_bits(hi[j])};
+                mma16n8k8_tf32(d[j], af, bf);
+            }
+        }
+    }
+    // this thread's results: rows g (and g + 8), value columns c0 + 8 t4 + e:
+    // e < 4 from tile e's first column pair entry, e >= 4 from tile e - 4's second
+    float* part0 = &sm.v[g][c0 + 8 * t4];
+    if (kh == 0) {
+        *reinterpret_cast<float4 *>(part0) = make_float4(d[0][0], d[1][0], d[2][0], d[3][0]);
+        *reinterpret_cast<float4 *>(part0 + 4) = make_float4(d[0][1], d[1][1], d[2][1], d[3][1]);
+        if (GM == 16) {
+            float *p1 = &sm.v[(g + 8) % GM][c0 + 8 * t4];
+            *reinterpret_cast<float4 *>(p1) = make_float4(d[0][2], d[1][2], d[2][2], d[3][2]);
+            *reinterpret_cast<float4 *>(p1 + 4) = make_float4(d[0][3], d[1][3], d[2][3], d[3][3]);
+        }
+    }
+    __syncthreads();
+    if (kh == 1) {
+#pragma unroll
+        for (int hr = 0; hr < (GM == 16 ? 2 : 1); ++hr) {
+            const int r = g + 8 * hr;
+            if (r < G) {
+                const float *p0 = &sm.v[r][c0 + 8 * t4];
+                const float *nn = &sm.kn[r][c0 + 8 * t4];
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float mine = e < 4 ? d[e][2 * hr] : d[e - 4][2 * hr + 1];
+                    y[e] = a.scale * ((p0[e] + mine) + nn[e]);
+                }
+                uint4 w;
+                w.x = pack_bf2(y[0], y[1]);
+                w.y = pack_bf2(y[2], y[3]);
+                w.z = pack_bf2(y[4], y[5]);
+                w.w = pack_bf2(y[6], y[7]);
+                *reinterpret_cast<uint4 *>((T *)a.o + ((tok0 + r) * a.H + h) * VD + c0 + 8 * t4) = w;
+            }
+        }
+    }
+}
+
 template <typename T, int GM>
 __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -387,45 +521,16 @@ __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs
             n[r] = acc;
         }
     }
-    __syncthreads();
-    // M h0: thread (column c, half hf) sums over rows 64 hf .. 64 hf + 63 of h0,
-    // 16 rows' loads in flight at a time; each warp load is one 128-byte piece
-    // of a row.  Rows of M past G are zero.
-    const int hf = tid >> 7;
-    float acc[GM];
+    if constexpr (sizeof(T) == 2) {
+        if (tid >= KD) {
 #pragma unroll
-    for (int r = 0; r < GM; ++r) acc[r] = 0.f;
-    const float *hp = S0 + (size_t)(64 * hf) * VD + c;
-#pragma unroll 1
-    for (int k16 = 0; k16 < 4; ++k16) {
-        float hv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) hv[e] = __ldcs(hp + (size_t)(16 * k16 + e) * VD);
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-            const int kk = 64 * hf + 16 * k16 + 4 * e4;
-#pragma unroll
-            for (int r = 0; r < GM; ++r) {
-                if (r < G) {
-                    const float4 m = *reinterpret_cast<const float4 *>(&sm.qg[r][kk]);
-                    acc[r] = fmaf(m.x, hv[4 * e4], acc[r]);
-                    acc[r] = fmaf(m.y, hv[4 * e4 + 1], acc[r]);
-                    acc[r] = fmaf(m.z, hv[4 * e4 + 2], acc[r]);
-                    acc[r] = fmaf(m.w, hv[4 * e4 + 3], acc[r]);
-                }
-            }
+            for (int r = 0; r < GM; ++r) sm.kn[r][c] = n[r];   // N, for the threads that store o
         }
-    }
-    if (hf == 0) {
-#pragma unroll
-        for (int r = 0; r < GM; ++r) sm.v[r][c] = acc[r];
-    }
-    __syncthreads();
-    if (hf == 1) {
-#pragma unroll
-        for (int r = 0; r < GM; ++r)
-            if (r < G)
-                ((T *)a.o)[((tok0 + r) * a.H + h) * VD + c] = from_f<T>(a.scale * ((sm.v[r][c] + acc[r]) + n[r]));
+        __syncthreads();
+        verify_product_mma<T, GM>(a, sm, S0, tok0, G, h, warp, lane);
+    } else {
+        __syncthreads();
+        verify_product_fma<T, GM>(a, sm, S0, tok0, G, h, n);
     }
 }
 
