@@ -222,6 +222,11 @@ KDA_API int kda_decode_step(kda_dtype dt, int B, int H, int K, int V, const void
  *   ring       host pointer to this layer's ring descriptor (device buffers)
  *   ring_base  device int32 [B] or NULL (= 0): ring entry of draft step 0
  * Requires 1 <= G <= ring->ring_len / 2.
+ * Arithmetic: the records are the decode step's values bit for bit (k, v as
+ * given, exp(gk) and beta in fp32).  o is formed from the committed state in
+ * one product; for bf16 inputs that product takes TF32 operands (rounded to
+ * nearest, inside the bf16 output's tolerance), for fp32 inputs it is fp32
+ * throughout.
  */
 KDA_API int kda_verify_store_inputs(kda_dtype dt, int B, int G, int H, int K, int V,
                                     const void *q, const void *k, const void *v, const void *gk,

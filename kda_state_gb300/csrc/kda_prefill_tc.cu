@@ -2,57 +2,66 @@
 //
 // One CTA (512 threads) per (sequence, head) unit walks the sequence in chunks
 // of C = 64 tokens with the fp32 128 x 128 state held in registers across
-// chunks; every chunk-sized contraction runs as a tcgen05.mma (bf16 operands
-// in shared memory, fp32 accumulators in TMEM).  The pages' FlashKDA fuses a
-// chunk's work and the state update into one kernel with intermediates on
-// chip (Kimi K3 on B200 deployment notes, timeline entry "FlashKDA"); its CuTe
-// rewrite keeps the state on chip and issues the longest sequences first.  Both
-// ideas are kept here; the chunk size, the state placement (registers, not
-// TMEM) and the work split are this kernel's own.
+// chunks (32 values per thread); every chunk-sized contraction runs as a
+// tcgen05.mma (operands in shared memory, fp32 accumulators in TMEM).  The
+// pages' FlashKDA fuses a chunk's work and the state update into one kernel
+// with intermediates on chip (Kimi K3 on B200 deployment notes, timeline entry
+// "FlashKDA"); its CuTe rewrite keeps the state on chip and issues the longest
+// sequences first.  Both ideas are kept here; the chunk size, the state
+// placement (registers, not TMEM) and the work split are this kernel's own.
 //
 // Chunk algebra (derived from the recurrence
 //     S_t = (I - b_t k_t k_t^T) Diag(exp(gk_t)) S_{t-1} + b_t k_t v_t^T,  o_t = S_t^T q_t
 // by unrolling it over the chunk).  With G_r = sum_{j<=r} gk_j per key channel,
-// S0 the state entering the chunk and the last row's G_L:
-//     A[r][j]  = b_r <k_r, exp(G_r - G_j) . k_j>  (j < r),  T = (I + A)^-1
-//     W        = T Diag(b) (K . exp(G)),   U~ = T Diag(b) V
-//     U        = U~ - W S0
-//     O        = (Q . exp(G)) S0 + Aqk U,  Aqk[r][j] = <q_r, exp(G_r - G_j) . k_j> (j <= r)
-//     S_L      = Diag(exp(G_L)) S0 + (K . exp(G_L - G))^T U
-// The pairwise factors exp(G_r - G_j) are split as exp(G_r - G_ref) *
-// exp(G_ref - G_j) around the chunk's middle row, which keeps both factors in
-// fp32 range while a key channel's decay over half a chunk stays within 80.
+// S0 the state entering the chunk, G_L the last row's G, K~ = K . exp(G),
+// Q~ = Q . exp(G) and K_end = K . exp(G_L - G):
+//     A[r][j]   = b_r <k_r, exp(G_r - G_j) . k_j>  (j < r),  T = (I + A)^-1
+//     Aqk[r][j] = <q_r, exp(G_r - G_j) . k_j>       (j <= r)
+//     U         = T Diag(b) (V - K~ S0)
+//     O         = Q~ S0 + Aqk U
+//     S_L       = Diag(exp(G_L)) S0 + K_end^T U
+// (U is the usual U~ - W S0 with U~ = T Diag(b) V and W = T Diag(b) K~, taken
+// in one product.)  The pairwise factors exp(G_r - G_j) of the Gram matrices
+// are split as exp(G_r - G_ref) * exp(G_ref - G_j) around the chunk's row 31,
+// which keeps both factors in fp32 range while a key channel's decay over half
+// a chunk stays within 79 (natural log).
+//
+// Per chunk (M = 128 throughout; shared-memory operands in the 128-byte-
+// swizzled canonical layouts):
+//   G1  [Kf; Qr] (128x128) x Kb^T   (tf32)  -> TMEM cols [0,64): A (rows 0-63), Aqk (64-127)
+//   P   [K~; Q~] (128x128) x S0     (fp16)  -> cols 256.. (by chunk parity): K~ S0, Q~ S0
+//   U   [T Diag(b); Aqk] (128x64) x V'      -> cols [0,128), rows 0-63 kept; V' = V - K~ S0
+//   G4a [T Diag(b); Aqk] (128x64) x U (+=)  -> P's rows 64-127 become O
+//   G4b K_end^T (128x64) x U                -> cols [0,128): the state increment
+// P depends on the previous chunk's state only, so it is issued with G1 and
+// read out (into V', in place of v) while the triangular solve runs; O stays in
+// TMEM until the next chunk's solve phase, where the warps of lanes 64..127
+// write it out.  CUDA cores do the cumulative decays and exponentials (prep),
+// the 64x64 unit-lower-triangular inverse (16x16 blocks: substitution on the
+// diagonal, warp-level TF32 MMAs off it), the TMEM read-outs and the fp32 state
+// update.
+//
+// Operand precision: the Gram factors span exp(+-26) and need an 8-bit
+// exponent, so G1 runs on TF32 (fp32 operand tiles); the operands of P, U and
+// G4 are bounded or checked (|.| <= 1 for the decayed q, k and Aqk; |q|, |k| <=
+// 256; T Diag(b), V', U and S below 60000) and use fp16's 11-bit significand.
+// All operands in bf16 would give about 3e-2 x RMS on o; this mix about 8e-3
+// (a CPU model of the chunk algebra with the kernel's roundings).
 //
 // Exactness over the whole input domain: a chunk whose factors or operands
-// would leave the formats below (that decay bound, a positive gk, |q| or |k|
-// above 256, Aqk, W, U or S above 60000) does not use the tensor-core result:
-// all 512 threads apply the recurrence to it token by token in fp32 on the
-// CUDA cores, from the state entering the chunk (still in registers: every
-// check is decided before the chunk's state update).
+// would leave those formats (the decay bound, a positive gk, |q| or |k| above
+// 256, Aqk, T Diag(b), V', U or S above 60000, or a NaN) does not use the
+// tensor-core result: all 512 threads apply the recurrence to it token by
+// token in fp32 on the CUDA cores, from the state entering the chunk (still in
+// registers: every check is decided before the chunk's state update).
 //
-// Per chunk, five groups of MMAs (M = 128 throughout; shared-memory operands
-// in the 128-byte-swizzled canonical layouts):
-//   G1  [Kf; Qr] (128x128) x Kb^T           -> TMEM cols [0,64):   A (rows 0-63), Aqk (64-127)
-//   G2  [T Diag(b); 0] (128x64) x [K~ | V]  -> cols [0,128): W,  cols [128,256): U~
-//   G3  [-W; Q~] (128x128) x S0 (+=)        -> cols [128,256): U (rows 0-63), Q~ S0 (64-127)
-//   G4a [0; Aqk] (128x64) x U (+=)          -> cols [128,256): rows 64-127 become O
-//   G4b (K . exp(G_L - G))^T (128x64) x U   -> cols [0,128): the state increment
-// Operand precision: the Gram factors span exp(+-26) and need an 8-bit
-// exponent, so G1 runs on TF32 (fp32 operands, 11-bit significands); G2 takes V
-// as given (bf16); the operands of G3 and G4 are bounded (|.| <= 1 for the
-// decayed q, k and Aqk; U, W and S are checked against 60000) and use fp16's
-// 11-bit significand.  Rounding all operands to bf16 instead gives 3e-2 x RMS
-// on o; this mix about 3e-3.
-// CUDA cores do the cumulative decays, the exponentials, the 64x64 unit-lower
-// triangular inverse (16x16 blocks), the TMEM read-outs and the fp32 state
-// update.  All waits are bounded (barrier_wait_for, the wait loop of the
-// library's other kernels); a wait that gives up reports KDA_DEVERR_TIMEOUT,
-// frees TMEM and abandons the unit without writing its slots.
-// Data movement around the phases: raw q, k, gk, v tiles arrive by TMA one
-// chunk ahead and are taken into registers while the previous chunk's G4 runs;
-// a chunk's O stays in TMEM until the next chunk's solve phase, where the warps
-// of lanes 64..127 write it with 32 x 32 tensor stores; the unit's initial and
-// final states move as whole 512-byte rows through a swizzled staging tile.
+// All waits are bounded (barrier_wait_for, the wait loop of the library's
+// other kernels, with a per-launch limit); a wait that gives up reports
+// KDA_DEVERR_TIMEOUT, frees TMEM and abandons the unit without writing its
+// slots.  Data movement: raw q, k, gk, v tiles arrive by TMA one chunk ahead
+// and are taken into registers while the previous chunk's G4 runs; the unit's
+// initial state arrives by four tensor copies into a swizzled staging tile and
+// the final state leaves as whole 512-byte rows through it.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -105,7 +114,7 @@ constexpr uint32_t OP_A3 = 131072;     // [K~; Q~] = [K; Q] . exp(G), fp16, 128 
 constexpr uint32_t OP_S = 163840;      // S0, fp16, 128 rows (k) x 128 (v), MN-major B
 constexpr uint32_t OP_KE = 196608;     // K . exp(G_L - G), fp16, 64 tokens x 128 ch, MN-major A
 constexpr uint32_t OP_U = 212992;      // U, fp16, 64 tokens x 128 v, MN-major B
-constexpr uint32_t SCR_T = OP_U;       // before G3: fp32 T [64][64]
+constexpr uint32_t SCR_T = OP_U;       // during the solve: fp32 T [64][64] (before U is read out)
 // Before the first chunk and after the last, the fp32 state passes through a
 // 64 KB staging tile here (KT, [-W; Q~] and the first half of S0).  In: four
 // tensor copies, box j = columns 32j .. 32j+31 of the 128 rows, 128 bytes per

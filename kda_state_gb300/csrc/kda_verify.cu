@@ -95,9 +95,9 @@ __global__ void __launch_bounds__(CTA_THREADS, 2) verify_kernel(VerifyArgs a) {
 // M and N depend on the draft alone, so h0 enters one G x 128 x 128 product
 // that streams h0 once from L2: a bulk prefetch asks for it when the unit
 // starts, and nothing of h0 is staged in shared memory.  For bf16 inputs the
-// product runs as warp-level TF32 MMAs (operands rounded to nearest; about
-// 1e-3 of RMS on o, within the bf16 output's bound), for fp32 inputs as fp32
-// FMAs.  A unit whose decay products over the draft leave
+// product runs as warp-level TF32 MMAs (operands rounded to nearest, within the
+// bf16 output's bound), for fp32 inputs as fp32 FMAs (the fp32 bound is beyond
+// TF32).  A unit whose decay products over the draft leave
 // (1e-30, 1e30), where k / E stops being exact in fp32, takes the recurrence
 // instead (verify_unit_sliced).
 template <int GM>
