@@ -112,7 +112,6 @@ struct VerifyBlockSmem {
     float kq[GM];       // recurrent path: k . q per token
     float red[2][8][32];   // recurrent path: partial sums of S'^T k and S'^T q
     float u[32];
-    int fallback;
 };
 
 // ---------------------------------------------------------------------------
@@ -411,15 +410,12 @@ __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs
     if (G == 0) return;
     // h0 (read-only): into L2 now, read once by the final product
     const float *S0 = a.pool + ((size_t)slot * a.H + h) * STATE_ELEMS;
-    if (tid == 0) {
-        sm.fallback = 0;   // set by the staging below, after the barrier
-        prefetch_l2(S0, STATE_ELEMS * sizeof(float));
-    }
-    __syncthreads();
+    if (tid < 4) prefetch_l2(S0 + tid * (STATE_ELEMS / 4), STATE_ELEMS);   // four 16 KB requests
     const int base = a.ring_base ? a.ring_base[b] : 0;
     const int mask = a.ring_len - 1;
     // stage the draft, store the records; running decay products per channel.
     // All loads of the draft are issued before the first store.
+    bool tiny = false;
     if (tid < KD) {
         const int c = tid;
         T kr[GM], qr[GM], gr[GM];
@@ -433,7 +429,6 @@ __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs
             }
         }
         float E = 1.f;
-        bool tiny = false;
 #pragma unroll
         for (int i = 0; i < GM; ++i) {
             if (i < G) {
@@ -449,7 +444,6 @@ __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs
                 sm.qg[i][c] = qq * E;
             }
         }
-        if (tiny) sm.fallback = 1;
     } else {
         const int c = tid - KD;
         T vr[GM], br[GM];
@@ -475,8 +469,7 @@ __global__ void __launch_bounds__(CTA_THREADS, 4) verify_block_kernel(VerifyArgs
             }
         }
     }
-    __syncthreads();
-    if (sm.fallback) {   // uniform: read after the barrier
+    if (__syncthreads_or(tiny)) {   // uniform
         verify_unit_sliced<T, GM>(a, sm, S0, tok0, G, h);
         return;
     }
