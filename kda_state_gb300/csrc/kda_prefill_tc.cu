@@ -87,7 +87,8 @@ constexpr uint32_t OP_KBT = 49152;     // Kb^T: 128 rows (k) x 32 tokens, one bo
 constexpr uint32_t RAW_V = 65536;      // raw bf16 v (TMA), 2 boxes of 4 KB
 constexpr uint32_t OP_TB = 73728;      // T Diag(b) by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of U)
 constexpr uint32_t OP_AQ = 81920;      // Aqk by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of O)
-constexpr uint32_t SCR_A = 90112;      // fp32 A [32][AS] (strictly lower, rows x beta)
+constexpr uint32_t OP_OST = 90112;     // o of a full chunk (bf16, 2 boxes of 64 ch x 32 tokens, SW128) for its tensor store
+constexpr uint32_t SCR_A = 98304;      // fp32 A [32][AS] (strictly lower, rows x beta)
 constexpr uint32_t SCR_T = SCR_A + 32 * AS * 4;   // fp32 T of the diagonal blocks [32][TS]
 constexpr int TS = 20;                             // its row stride (floats)
 constexpr uint32_t SCR_R = SCR_T + 32 * TS * 4;    // fp32 R = A_10 T_00 [16][TS]
@@ -103,6 +104,7 @@ constexpr uint32_t SM_MISC = SM_BAR + 128;         // TMEM base
 constexpr uint32_t SMEM_USED = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SCR_A % 16 == 0 && SCR_T % 16 == 0 && SCR_R % 16 == 0 && FB_IN % 16 == 0, "scratch misaligned");
+static_assert(OP_OST % 1024 == 0, "the o staging tile must be 1024-aligned for its 128-byte swizzle");
 static_assert(SM_ELR % 16 == 0 && SM_TOT % 16 == 0, "factor arrays misaligned");
 static_assert(RAW_G + 8192 <= OP_KB, "raw tiles overflow the Gram operand tile");
 static_assert(OP_TB % 1024 == 0 && OP_AQ % 1024 == 0 && OP_KBT % 1024 == 0, "operand tiles misaligned");
@@ -116,12 +118,12 @@ constexpr uint32_t TM_G = 192;   // the Gram product (M = 64 layout), 32 columns
 constexpr uint32_t TM_U = 224;   // U^T, 32 columns
 
 constexpr uint64_t WAIT_NS = 2000000000ull;   // bounded waits: 2 s
-constexpr float K_LIMIT = 256.f;              // |k| bound of the tensor-core path
+constexpr unsigned K_LIMIT_BITS = 0x4380u;    // |k| bound of the tensor-core path: 256 as bf16 bits
 constexpr float D_LIMIT = 60.f;               // decay over a chunk (natural log)
 constexpr float U_LIMIT = 1.0e6f;             // max |T Diag(b)| x max |V'|
 
 struct Params {
-    CUtensorMap tq, tk, tg, tv;   // [T][H][128] bf16: boxes of 64 channels x 1 head x 32 tokens
+    CUtensorMap tq, tk, tg, tv, to;   // [T][H][128] bf16: boxes of 64 channels x 1 head x 32 tokens
     int N, T_total, H, num_slots, lpt;
     const __nv_bfloat16 *beta;
     const int32_t *cu;
@@ -159,6 +161,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Bulk tensor store of a shared-memory box; completes in this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -353,7 +367,7 @@ __device__ __forceinline__ float solve32(uint8_t *sm, uint8_t *tb, const float *
         for (int r = 0; r < 16; ++r) {
             const int rr = 16 * I + r;
             Ts[rr * TS + col] = x[r];
-            const float tv = tf32r(x[r] * bc);
+            const float tv = x[r] * bc;
             tmax = maxnan3(tmax, fabsf(tv), 0.f);
             *reinterpret_cast<float *>(tb + off_sq(rr, c)) = tv;
         }
@@ -394,8 +408,8 @@ __device__ __forceinline__ float solve32(uint8_t *sm, uint8_t *tb, const float *
         }
         const int c = 8 * nt + 2 * t4;
         const float b0 = beta[c], b1 = beta[c + 1];
-        const float2 lo = make_float2(tf32r(-d[0] * b0), tf32r(-d[1] * b1));
-        const float2 hi = make_float2(tf32r(-d[2] * b0), tf32r(-d[3] * b1));
+        const float2 lo = make_float2(-d[0] * b0, -d[1] * b1);
+        const float2 hi = make_float2(-d[2] * b0, -d[3] * b1);
         tmax = maxnan3(tmax, maxnan3(fabsf(lo.x), fabsf(lo.y), fabsf(hi.x)), fabsf(hi.y));
         *reinterpret_cast<float2 *>(tb + off_sq(16 + g, c)) = lo;
         *reinterpret_cast<float2 *>(tb + off_sq(24 + g, c)) = hi;
@@ -614,7 +628,12 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             //     after which the operand tiles are written over them.
             float gv[2][4][4];
             uint2 wq[2][4], wk[2][4];
-            float gmax = 0.f, kmax = 0.f;
+            // checks on the raw bf16 bits, two at a time: the largest |k| as an
+            // unsigned magnitude (a NaN is above every finite value), the largest
+            // gk as a signed 16-bit integer (> 0 only for a positive gk or a NaN
+            // with the sign clear; other NaNs reach the decay check through G)
+            unsigned kbits = 0u;
+            int gbits = (int)0x80008000u;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int k0 = 4 * cg + 64 * hf;
@@ -628,10 +647,8 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const uint2 wg = *reinterpret_cast<const uint2 *>(sm + (valid ? RAW_G + ro : SM_ZERO));
                     gv[hf][i][0] = bf16_lo(wg.x); gv[hf][i][1] = bf16_hi(wg.x);
                     gv[hf][i][2] = bf16_lo(wg.y); gv[hf][i][3] = bf16_hi(wg.y);
-                    gmax = maxnan3(gmax, maxnan3(gv[hf][i][0], gv[hf][i][1], gv[hf][i][2]), gv[hf][i][3]);
-                    kmax = maxnan3(kmax, maxnan3(fabsf(bf16_lo(wk[hf][i].x)), fabsf(bf16_hi(wk[hf][i].x)),
-                                                 fabsf(bf16_lo(wk[hf][i].y))),
-                                   fabsf(bf16_hi(wk[hf][i].y)));
+                    gbits = __vmaxs2(gbits, __vmaxs2((int)wg.x, (int)wg.y));
+                    kbits = __vmaxu2(kbits, __vmaxu2(wk[hf][i].x & 0x7FFF7FFFu, wk[hf][i].y & 0x7FFF7FFFu));
                 }
                 // inclusive prefix over the thread's 4 rows, then over the two
                 // row groups of the octet (lanes l and l ^ 16)
@@ -687,14 +704,16 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const float2 kt01 = __fmul2_rn(k01, ef[0]), kt23 = __fmul2_rn(k23, ef[1]);
                     const float2 qt01 = __fmul2_rn(q01, ef[0]), qt23 = __fmul2_rn(q23, ef[1]);
                     const float2 kb01 = __fmul2_rn(k01, eb[0]), kb23 = __fmul2_rn(k23, eb[1]);
-                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(r, k0, 64)) = tf32r4(kt01.x, kt01.y, kt23.x, kt23.y);
+                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(r, k0, 64)) = make_float4(kt01.x, kt01.y, kt23.x, kt23.y);
                     *reinterpret_cast<float4 *>(sm + OP_QR + off32(32 + r, k0, 64)) =
                         tf32r4(qt01.x, qt01.y, qt23.x, qt23.y);
                     *reinterpret_cast<float4 *>(sm + OP_KB + off32(r, k0, 32)) = tf32r4(kb01.x, kb01.y, kb23.x, kb23.y);
                 }
             }
             fence_proxy_async();   // the tiles are read by the tensor cores
-            const int bad = !(dmax <= D_LIMIT * LOG2E) || !(gmax <= 0.f) || !(kmax <= K_LIMIT);
+            const int gtop = max((int)(short)(gbits & 0xFFFF), (int)(short)((unsigned)gbits >> 16));
+            const unsigned ktop = max(kbits & 0xFFFFu, kbits >> 16);
+            const int bad = !(dmax <= D_LIMIT * LOG2E) || gtop > 0 || ktop > K_LIMIT_BITS;
             if (named_or(1, 128, tmo)) { aborted = true; break; }
             const int fb1 = named_or(1, 128, bad);
             if (tid == 0) fbf[pc] = fb1;
@@ -824,16 +843,19 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const uint32_t vb = RAW_V + (v >> 6) * (C * 128) + (v & 7) * 2;
                     const int cv = (v >> 3) & 7;
                     float vm = 0.f;
+                    // rows past the sequence (a partial chunk only) are zero
+                    const int lim = L == C ? 32 : L;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t r[16];
                         KDA_TMEM_LD16(lane_base + TM_P + 16 * hf, r);
                         const uint8_t *vrow = sm + vb + 16 * hf * 128;
+                        const int lh = lim - 16 * hf;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const uint16_t bits = *reinterpret_cast<const uint16_t *>(vrow + i * 128 + (((cv ^ i) & 7) << 4));
-                            const float vp =
-                                16 * hf + i < L ? __uint_as_float((uint32_t)bits << 16) - __uint_as_float(r[i]) : 0.f;
+                            float vp = __uint_as_float((uint32_t)bits << 16) - __uint_as_float(r[i]);
+                            if (i >= lh) vp = 0.f;
                             vm = maxnan3(vm, fabsf(vp), 0.f);
                             r[i] = to_tf32(vp);
                         }
@@ -891,16 +913,42 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 if (cs >= 0) ckd = p.pool + ((size_t)cs * p.H + h) * STATE_ELEMS;
             }
             if (tc_path) {
-                // (6) O out (rows 0..31 of column v); the next chunk's state
-                //     S = Diag(exp(G_L)) X (and a checkpoint of it)
+                // (6) O out (rows 0..31 of column v): a full chunk through the
+                //     staging tile and two tensor stores, a partial one directly;
+                //     then the next chunk's state S = Diag(exp(G_L)) X (and a
+                //     checkpoint of it)
+                if (L == C) {
+                    if (leader) bulk_wait_read();   // the previous chunk's o has left the staging tile
+                    named_sync(2, 128);
+                    const uint32_t ob = OP_OST + (v >> 6) * (C * 128) + (v & 7) * 2;
+                    const int cv = (v >> 3) & 7;
 #pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t r[16];
-                    KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
-                    __nv_bfloat16 *dst = p.o + ((size_t)(t0 + 16 * hf) * p.H + h) * VD + v;
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t r[16];
+                        KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
+                        uint8_t *orow = sm + ob + 16 * hf * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (16 * hf + i < L) dst[(size_t)i * p.H * VD] = __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
+                        for (int i = 0; i < 16; ++i)
+                            *reinterpret_cast<__nv_bfloat16 *>(orow + i * 128 + (((cv ^ i) & 7) << 4)) =
+                                __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
+                    }
+                    fence_proxy_async();
+                    named_sync(2, 128);
+                    if (leader) {
+                        tma_store_3d(&p.to, sbase + OP_OST, 0, h, t0);
+                        tma_store_3d(&p.to, sbase + OP_OST + C * 128, 64, h, t0);
+                        bulk_commit();
+                    }
+                } else {
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t r[16];
+                        KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
+                        __nv_bfloat16 *dst = p.o + ((size_t)(t0 + 16 * hf) * p.H + h) * VD + v;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (16 * hf + i < L) dst[(size_t)i * p.H * VD] = __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
+                    }
                 }
                 const float *f = elr + par * 128;
 #pragma unroll 1
@@ -939,6 +987,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             tc_fence_before();
             barrier_arrive(bar_done);   // (7) chunk c is done: its tiles and parity buffers may be reused
         }
+        if (leader) bulk_wait_all();   // every o tensor store is complete
         // the final state, unless a wait gave up
         if (!aborted) {
             tc_fence_after();
@@ -1005,7 +1054,8 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s) {
     memset(&p, 0, sizeof(p));
     if (a.T_total > 0) {
         if (!make_map(&p.tq, a.q, a.H, a.T_total) || !make_map(&p.tk, a.k, a.H, a.T_total) ||
-            !make_map(&p.tg, a.gk, a.H, a.T_total) || !make_map(&p.tv, a.v, a.H, a.T_total))
+            !make_map(&p.tg, a.gk, a.H, a.T_total) || !make_map(&p.tv, a.v, a.H, a.T_total) ||
+            !make_map(&p.to, a.o, a.H, a.T_total))
             return cudaErrorInvalidValue;
     }
     p.N = a.N; p.T_total = a.T_total; p.H = a.H; p.num_slots = a.num_slots;
