@@ -310,6 +310,10 @@ __device__ __forceinline__ float maxnan3(float a, float b, float c) {
     asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ void mma_m16n8k8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
@@ -808,6 +812,40 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             }
         }
         uint32_t n_p = 0, n_u = 0;   // chunks whose P / U were issued
+        // O of the previous tensor-core chunk, held in registers (bf16 pairs,
+        // rows 2i and 2i + 1 of column v) so that it leaves while the next
+        // chunk's P runs: a full chunk through the staging tile and two tensor
+        // stores, a partial one by direct stores
+        uint32_t opk[16];
+        bool o_pend = false;
+        int o_t0 = 0, o_L = 0;
+        auto flush_o = [&]() {
+            if (!o_pend) return;
+            o_pend = false;
+            if (o_L == C) {
+                if (leader) bulk_wait_read();   // the previous tensor store has read the staging tile
+                named_sync(2, 128);
+                const uint32_t ob = OP_OST + (v >> 6) * (C * 128) + (v & 7) * 2;
+                const int cv = (v >> 3) & 7;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint16_t bits = (uint16_t)(i & 1 ? opk[i >> 1] >> 16 : opk[i >> 1] & 0xFFFFu);
+                    *reinterpret_cast<uint16_t *>(sm + ob + i * 128 + (((cv ^ i) & 7) << 4)) = bits;
+                }
+                fence_proxy_async();
+                named_sync(2, 128);
+                if (leader) {
+                    tma_store_3d(&p.to, sbase + OP_OST, 0, h, o_t0);
+                    tma_store_3d(&p.to, sbase + OP_OST + C * 128, 64, h, o_t0);
+                    bulk_commit();
+                }
+            } else {
+                unsigned short *dst = reinterpret_cast<unsigned short *>(p.o) + ((size_t)o_t0 * p.H + h) * VD + v;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < o_L) dst[(size_t)i * p.H * VD] = (unsigned short)(i & 1 ? opk[i >> 1] >> 16 : opk[i >> 1] & 0xFFFFu);
+            }
+        };
         for (int c = 0; c < nchunks; ++c) {
             const int t0 = bos + c * C;
             const int L = min(C, eos - t0);
@@ -830,6 +868,9 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                         mma_ts(tmem + TM_P, tmem + TM_X + 8 * s, da + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4),
                                ID_P, s > 0);
                     mma_commit(bar_p);
+                }
+                flush_o();   // the previous chunk's O, while P runs
+                if (leader) {
                     if (!barrier_wait_for(bar_p, ppar, wait_ns) || !barrier_wait_for(bar_g1, ppar, wait_ns) ||
                         !barrier_wait_for(bar_v, par, wait_ns))
                         tmo = 1;
@@ -913,43 +954,20 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 if (cs >= 0) ckd = p.pool + ((size_t)cs * p.H + h) * STATE_ELEMS;
             }
             if (tc_path) {
-                // (6) O out (rows 0..31 of column v): a full chunk through the
-                //     staging tile and two tensor stores, a partial one directly;
-                //     then the next chunk's state S = Diag(exp(G_L)) X (and a
-                //     checkpoint of it)
-                if (L == C) {
-                    if (leader) bulk_wait_read();   // the previous chunk's o has left the staging tile
-                    named_sync(2, 128);
-                    const uint32_t ob = OP_OST + (v >> 6) * (C * 128) + (v & 7) * 2;
-                    const int cv = (v >> 3) & 7;
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t r[16];
-                        KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
-                        uint8_t *orow = sm + ob + 16 * hf * 128;
+                // (6) O of the chunk into registers (it leaves during the next
+                //     chunk's P); then the next chunk's state S = Diag(exp(G_L)) X
+                //     (and a checkpoint of it)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            *reinterpret_cast<__nv_bfloat16 *>(orow + i * 128 + (((cv ^ i) & 7) << 4)) =
-                                __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
-                    }
-                    fence_proxy_async();
-                    named_sync(2, 128);
-                    if (leader) {
-                        tma_store_3d(&p.to, sbase + OP_OST, 0, h, t0);
-                        tma_store_3d(&p.to, sbase + OP_OST + C * 128, 64, h, t0);
-                        bulk_commit();
-                    }
-                } else {
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t r[16];
-                        KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
-                        __nv_bfloat16 *dst = p.o + ((size_t)(t0 + 16 * hf) * p.H + h) * VD + v;
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t r[16];
+                    KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (16 * hf + i < L) dst[(size_t)i * p.H * VD] = __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        opk[8 * hf + i] = pack_bf16x2(p.scale * __uint_as_float(r[2 * i]), p.scale * __uint_as_float(r[2 * i + 1]));
                 }
+                o_pend = true;
+                o_t0 = t0;
+                o_L = L;
                 const float *f = elr + par * 128;
 #pragma unroll 1
                 for (int g = 0; g < 4; ++g) {
@@ -980,6 +998,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     if (c + 1 < nchunks) load_v(t0 + C);
                 }
                 if (named_or(2, 128, tmo)) { aborted = true; break; }
+                flush_o();
                 tc_fence_after();
                 chunk_recurrent(p, sm, lane_base, v, t0, L, h);
                 if (ckd) store_state(ckd, lane_base, v);
@@ -987,6 +1006,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             tc_fence_before();
             barrier_arrive(bar_done);   // (7) chunk c is done: its tiles and parity buffers may be reused
         }
+        if (!aborted) flush_o();
         if (leader) bulk_wait_all();   // every o tensor store is complete
         // the final state, unless a wait gave up
         if (!aborted) {
