@@ -172,7 +172,7 @@ def varlen_workload(device, seed=1, H=64):
 
 
 NOMINAL_HBM_GBS = 8000.0   # the nominal HBM3e bandwidth the fractions are also quoted against
-CHUNK = 64                 # chunk length of the tensor-core prefill
+CHUNK = 32                 # chunk length of the tensor-core prefill
 
 
 def chunked_flops_per_token_head(C=CHUNK, d=KD):
