@@ -78,9 +78,9 @@ enum {
     KDA_DEVERR_SEQLENS = 4,      /* cu_seqlens or cu_drafts not monotone or past total_tokens,
                                     or a draft count above G_max */
     KDA_DEVERR_RANGE = 8,        /* reserved: no kernel sets it.  The chunked prefill runs any
-                                    chunk whose values leave its tensor-core operand formats
-                                    (strong decays, positive gk, large q, k, v or state) through
-                                    an exact fp32 recurrence instead of reporting it */
+                                    chunk whose products could leave fp32 range (strong decays,
+                                    positive gk, large k, v or state) through an fp32 recurrence
+                                    instead of reporting it */
     KDA_DEVERR_TIMEOUT = 16      /* a kernel's bounded wait on its own copies gave up (the unit
                                     is abandoned, its slot is not written) */
 };
@@ -145,9 +145,9 @@ typedef struct {
  * bf16 runs the chunked tensor-core kernel; fp32 runs an exact fp32 kernel on
  * the CUDA cores.  Zero-length sequences copy init to out (or write zeros).
  * The chunked kernel is defined on every input the recurrence is: a chunk
- * whose decays or magnitudes leave its operand formats (a key channel's
- * log-decay over half a chunk beyond 80 in magnitude, a positive gk, |q| or
- * |k| above 256, |v| or an intermediate above 60000) is computed by the exact
+ * whose products could leave fp32 range (a key channel's log-decay over the
+ * 32-token chunk beyond 60 in magnitude, a positive gk, |k| above 256, a NaN,
+ * or max |T Diag(beta)| x max |V - K~ S| above 1e6) is computed by the
  * recurrence in fp32 instead, slower but within the same tolerance.  A unit
  * whose bounded wait gave up (KDA_DEVERR_TIMEOUT) writes none of its slots.
  */

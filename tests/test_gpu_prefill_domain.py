@@ -1,9 +1,9 @@
 """The bf16 chunked prefill over the whole input domain of the recurrence.
 
-The tensor-core path splits each pairwise decay factor exp(G_r - G_j) around
-a reference row and stores most operands in fp16; chunks whose values leave
-those formats (fast-forgetting key channels, a positive gk, large q, k, v or
-state) must still give the oracle's result.  Every case here is compared with
+The tensor-core path scales q and k by the chunk's cumulative decay exp(G) and
+k by exp(-G) (TF32 operands); chunks whose products could leave fp32 range
+(fast-forgetting key channels, a positive gk, large k, v or state) must still
+give the oracle's result.  Every case here is compared with
 the oracle at the bf16 tolerance; none may report an error, and the snapshot,
 checkpoint and canary slots obey the same contracts as on ordinary inputs.
 The prefill's own bounded wait is exercised through kda_selftest_prefill_wait.
@@ -91,7 +91,7 @@ def base_inputs(seed, lengths=LENGTHS, H=2):
 @pytest.mark.parametrize("lo,hi", [(3.0, 8.0), (8.0, 40.0)])
 def test_fast_forgetting_channels(lo, hi):
     """A few key channels decay by 3 to 40 nats per token: their log-decay over
-    half a chunk leaves the split factors' range."""
+    a chunk leaves the range of exp(-G)."""
     x, g = base_inputs(21)
     x["gk"] = strong_decay(x["gk"], g, [0, 5, 77, 127], lo, hi)
     run(x, LENGTHS, 2, seed=21)
@@ -139,10 +139,9 @@ def test_positive_log_decay():
 
 
 def test_large_q_v_k_and_state():
-    """Magnitudes beyond the tensor-core path's operand formats: |q| above 256
-    and |v| above 60000; |k| above 256 with beta scaled down so that
-    beta |k|^2 stays below 2 (the delta rule is stable only there); a
-    checkpoint above 60000."""
+    """Magnitudes far beyond the input recipe's: |q| x 400 and |v| x 70000; |k|
+    above 256 with beta scaled down so that beta |k|^2 stays below 2 (the
+    delta rule is stable only there); a checkpoint of 5e6."""
     x, _ = base_inputs(26)
     x["q"] = x["q"] * 400.0
     x["v"] = x["v"] * 7.0e4
