@@ -36,10 +36,12 @@
 // (16 x 16 blocks: substitution on the diagonal, warp-level TF32 MMAs off it),
 // V' = V - K~ S in TMEM, and the read-outs.  The next chunk's prep runs while
 // this chunk's U, O and state-update products are on the tensor cores.
-// Operand tiles written by the CUDA cores are rounded to TF32 (round to
-// nearest); the TMEM operands S and U are read by the tensor core as they are.
-// A CPU model of this data flow (the product roundings included) gives about
-// 4e-3 x RMS on o and 6e-3 on the state on the workload's inputs.
+// Kb and Aqk are rounded to TF32 to nearest by the CUDA cores that write them;
+// K~, Q~, V' and T Diag(b) are written unrounded, and they and the TMEM
+// operands S and U are truncated to TF32 by the tensor core.  A CPU model of
+// this data flow (the product roundings included) gives about 6e-3 x RMS on o
+// and 7e-3 on the state on the workload's inputs; Kb truncated as well would
+// take the state past 1e-2.
 //
 // Exactness over the whole input domain: a chunk whose factors could leave
 // fp32 range in the products (a decay above 60 nats over the chunk, a positive
@@ -710,7 +712,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const float2 kb01 = __fmul2_rn(k01, eb[0]), kb23 = __fmul2_rn(k23, eb[1]);
                     *reinterpret_cast<float4 *>(sm + OP_QR + off32(r, k0, 64)) = make_float4(kt01.x, kt01.y, kt23.x, kt23.y);
                     *reinterpret_cast<float4 *>(sm + OP_QR + off32(32 + r, k0, 64)) =
-                        tf32r4(qt01.x, qt01.y, qt23.x, qt23.y);
+                        make_float4(qt01.x, qt01.y, qt23.x, qt23.y);
                     *reinterpret_cast<float4 *>(sm + OP_KB + off32(r, k0, 32)) = tf32r4(kb01.x, kb01.y, kb23.x, kb23.y);
                 }
             }
@@ -898,7 +900,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                             float vp = __uint_as_float((uint32_t)bits << 16) - __uint_as_float(r[i]);
                             if (i >= lh) vp = 0.f;
                             vm = maxnan3(vm, fabsf(vp), 0.f);
-                            r[i] = to_tf32(vp);
+                            r[i] = __float_as_uint(vp);
                         }
                         KDA_TMEM_ST16(lane_base + TM_P + 16 * hf, r);
                     }
