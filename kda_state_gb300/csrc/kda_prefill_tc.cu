@@ -90,7 +90,7 @@ constexpr uint32_t RAW_V = 65536;      // raw bf16 v (TMA), 2 boxes of 4 KB
 constexpr uint32_t OP_TB = 73728;      // T Diag(b) by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of U)
 constexpr uint32_t OP_AQ = 81920;      // Aqk by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of O)
 constexpr uint32_t OP_OST = 90112;     // o of a full chunk (bf16, 2 boxes of 64 ch x 32 tokens, SW128) for its tensor store
-constexpr uint32_t SCR_A = 98304;      // fp32 A [32][AS] (strictly lower, rows x beta)
+constexpr uint32_t SCR_A = 98304;      // fp32 Diag(b) K~ Kb^T [32][AS]; A is its strictly lower part
 constexpr uint32_t SCR_T = SCR_A + 32 * AS * 4;   // fp32 T of the diagonal blocks [32][TS]
 constexpr int TS = 20;                             // its row stride (floats)
 constexpr uint32_t SCR_R = SCR_T + 32 * TS * 4;    // fp32 R = A_10 T_00 [16][TS]
@@ -334,9 +334,10 @@ __device__ __forceinline__ uint32_t off_sq(int r, int c) {
 // ---------------------------------------------------------------------------
 // 32 x 32 unit-lower-triangular inverse T = (I + A)^-1 by warps 0 and 1, and
 // T Diag(beta) into the B tile of U (its upper-right block stays zero from
-// the unit's set-up).  A is fp32 [32][AS] (strictly lower, rows scaled by
-// beta).  Warp I inverts diagonal block I by column-oriented forward
-// substitution (lane = column, lanes 16-31 idle); warp 0 then forms
+// the unit's set-up).  A is the strictly lower part of fp32 [32][AS] (rows
+// scaled by beta; nothing on or above the diagonal is read).  Warp I inverts
+// diagonal block I by column-oriented forward substitution (lane = column,
+// lanes 16-31 idle); warp 0 then forms
 // R = A_10 T_00, and after a two-warp barrier each warp forms one half of
 //     T_10 = -T_11 R
 // (warp-level m16n8k8 TF32 MMAs).  Returns this warp's largest |T Diag(beta)|
@@ -493,6 +494,30 @@ __device__ __forceinline__ void store_state(float *dst, uint32_t lane_base, int 
 #pragma unroll
         for (int e = 0; e < 32; ++e) __stcs(dst + (size_t)(32 * g + e) * VD + v, __uint_as_float(r[e]));
     }
+}
+
+// V' = V - K~ S for 16 tokens of this thread's value column, in place in TMEM
+// (columns taddr .. taddr + 15); vrow is the column's bytes in token row 0 of
+// the raw v tile (rows 128 B apart, 16-byte chunk index XOR the row).  With
+// MASK, tokens from lh on are past the sequence and give 0.  vm collects the
+// largest |V'| (NaN if any is NaN).
+template <bool MASK>
+__device__ __forceinline__ void vprime_half(const uint8_t *vrow, int cv, uint32_t taddr, int lh, float &vm) {
+    uint32_t r[16];
+    KDA_TMEM_LD16(taddr, r);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        float vp[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint16_t bits = *reinterpret_cast<const uint16_t *>(vrow + (i + e) * 128 + (((cv ^ (i + e)) & 7) << 4));
+            vp[e] = __uint_as_float((uint32_t)bits << 16) - __uint_as_float(r[i + e]);
+            if (MASK && i + e >= lh) vp[e] = 0.f;
+            r[i + e] = __float_as_uint(vp[e]);
+        }
+        vm = maxnan3(vm, fabsf(vp[0]), fabsf(vp[1]));
+    }
+    KDA_TMEM_ST16(taddr, r);
 }
 
 // ---------------------------------------------------------------------------
@@ -744,14 +769,17 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 if (lane < 16) {
                     const int row = 16 * (lq & 1) + lane;
                     if (lq < 2) {
+                        // the whole row, scaled by beta: the inverse reads only
+                        // the strictly lower part
                         const float b = beta_s[row];
                         float4 *dst = reinterpret_cast<float4 *>(As + row * AS);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            float a4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) a4[e] = (4 * j + e < row) ? __uint_as_float(r[4 * j + e]) * b : 0.f;
-                            dst[j] = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                            const float2 lo = __fmul2_rn(make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])),
+                                                         make_float2(b, b));
+                            const float2 hi = __fmul2_rn(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])),
+                                                         make_float2(b, b));
+                            dst[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
                         }
                     } else {
 #pragma unroll
@@ -887,22 +915,12 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const int cv = (v >> 3) & 7;
                     float vm = 0.f;
                     // rows past the sequence (a partial chunk only) are zero
-                    const int lim = L == C ? 32 : L;
+                    if (L == C) {
 #pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t r[16];
-                        KDA_TMEM_LD16(lane_base + TM_P + 16 * hf, r);
-                        const uint8_t *vrow = sm + vb + 16 * hf * 128;
-                        const int lh = lim - 16 * hf;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint16_t bits = *reinterpret_cast<const uint16_t *>(vrow + i * 128 + (((cv ^ i) & 7) << 4));
-                            float vp = __uint_as_float((uint32_t)bits << 16) - __uint_as_float(r[i]);
-                            if (i >= lh) vp = 0.f;
-                            vm = maxnan3(vm, fabsf(vp), 0.f);
-                            r[i] = __float_as_uint(vp);
-                        }
-                        KDA_TMEM_ST16(lane_base + TM_P + 16 * hf, r);
+                        for (int hf = 0; hf < 2; ++hf) vprime_half<false>(sm + vb + 16 * hf * 128, cv, lane_base + TM_P + 16 * hf, 16, vm);
+                    } else {
+#pragma unroll 1
+                        for (int hf = 0; hf < 2; ++hf) vprime_half<true>(sm + vb + 16 * hf * 128, cv, lane_base + TM_P + 16 * hf, L - 16 * hf, vm);
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) vm = maxnan3(vm, __shfl_xor_sync(0xffffffffu, vm, off), 0.f);
@@ -964,8 +982,11 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     uint32_t r[16];
                     KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        opk[8 * hf + i] = pack_bf16x2(p.scale * __uint_as_float(r[2 * i]), p.scale * __uint_as_float(r[2 * i + 1]));
+                    for (int i = 0; i < 8; ++i) {
+                        const float2 os = __fmul2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                                     make_float2(p.scale, p.scale));
+                        opk[8 * hf + i] = pack_bf16x2(os.x, os.y);
+                    }
                 }
                 o_pend = true;
                 o_t0 = t0;
