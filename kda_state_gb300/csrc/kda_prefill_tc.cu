@@ -804,22 +804,25 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             //     read the previous Kb^T); rebuilt from Kb
             if (tid == 0 && cc > 0 && !barrier_wait_for(bar_done, (uint32_t)((cc - 1) & 1), wait_ns)) tmo = 1;
             named_sync(1, 128);
+            {
+                // 4 x 4 blocks (tokens 4 l8.., channels 4 kq..), eight lanes of a
+                // phase on one diagonal: the loads and the stores each meet
+                // eight different 16-byte bank groups
+                const int l8 = tid & 7, q = tid >> 3;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int k0 = 4 * cg + 64 * hf;
-                float4 kr[4];
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int kq = (q + 16 * hf + l8) & 31;
+                    float4 kr[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    kr[i] = *reinterpret_cast<const float4 *>(sm + OP_KB + off32(8 * o8 + 4 * rg + i, k0, 32));
-                const int tc4 = 2 * o8 + rg;
-                *reinterpret_cast<float4 *>(sm + OP_KBT + (k0 + 0) * 128 + (((tc4 ^ (k0 + 0)) & 7) << 4)) =
-                    make_float4(kr[0].x, kr[1].x, kr[2].x, kr[3].x);
-                *reinterpret_cast<float4 *>(sm + OP_KBT + (k0 + 1) * 128 + (((tc4 ^ (k0 + 1)) & 7) << 4)) =
-                    make_float4(kr[0].y, kr[1].y, kr[2].y, kr[3].y);
-                *reinterpret_cast<float4 *>(sm + OP_KBT + (k0 + 2) * 128 + (((tc4 ^ (k0 + 2)) & 7) << 4)) =
-                    make_float4(kr[0].z, kr[1].z, kr[2].z, kr[3].z);
-                *reinterpret_cast<float4 *>(sm + OP_KBT + (k0 + 3) * 128 + (((tc4 ^ (k0 + 3)) & 7) << 4)) =
-                    make_float4(kr[0].w, kr[1].w, kr[2].w, kr[3].w);
+                    for (int i = 0; i < 4; ++i)
+                        kr[i] = *reinterpret_cast<const float4 *>(sm + OP_KB + off32(4 * l8 + i, 4 * kq, 32));
+                    uint8_t *dst = sm + OP_KBT + 4 * kq * 128;
+                    const int sw = 4 * (kq & 1);
+                    *reinterpret_cast<float4 *>(dst + 0 * 128 + ((l8 ^ (sw + 0)) << 4)) = make_float4(kr[0].x, kr[1].x, kr[2].x, kr[3].x);
+                    *reinterpret_cast<float4 *>(dst + 1 * 128 + ((l8 ^ (sw + 1)) << 4)) = make_float4(kr[0].y, kr[1].y, kr[2].y, kr[3].y);
+                    *reinterpret_cast<float4 *>(dst + 2 * 128 + ((l8 ^ (sw + 2)) << 4)) = make_float4(kr[0].z, kr[1].z, kr[2].z, kr[3].z);
+                    *reinterpret_cast<float4 *>(dst + 3 * 128 + ((l8 ^ (sw + 3)) << 4)) = make_float4(kr[0].w, kr[1].w, kr[2].w, kr[3].w);
+                }
             }
             fence_proxy_async();
             tc_fence_before();
