@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
     };
     if (tid == 0) {
         for (int b = 0; b < 6; ++b) mbar_init(bar_raw + 8 * b, 1);
-        for (int b = 6; b < 9; ++b) mbar_init(bar_raw + 8 * b, 128);
+        for (int b = 6; b < 9; ++b) mbar_init(bar_raw + 8 * b, 4);   // one arrival per warp of a group
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (nchunks > 0 && !p.skip_first_load) load_qkg(bos);
         if (nchunks > 0) load_v(bos);
@@ -612,6 +612,12 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
+    // one arrival for the warp, after every lane's earlier accesses (the warp
+    // barrier orders them before lane 0's release)
+    auto warp_arrive = [&](uint32_t bar) {
+        __syncwarp();
+        if (lane == 0) barrier_arrive(bar);
+    };
     const float LOG2E = 1.4426950408889634f;
     constexpr uint32_t ID_G1 = idesc_tf32(64, 32);
     constexpr uint32_t ID_P = idesc_tf32(128, 64);
@@ -748,7 +754,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             if (named_or(1, 128, tmo)) { aborted = true; break; }
             const int fb1 = named_or(1, 128, bad);
             if (tid == 0) fbf[pc] = fb1;
-            barrier_arrive(bar_tiles);   // (3) chunk cc's tiles (and its verdict) for the consumer
+            warp_arrive(bar_tiles);   // (3) chunk cc's tiles (and its verdict) for the consumer
             if (!fb1) {
                 // (4) G1 = [K~; Q~] Kb^T (M = 64); A, Aqk read out; T Diag(b)
                 if (tid == 0) {
@@ -826,7 +832,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             }
             fence_proxy_async();
             tc_fence_before();
-            barrier_arrive(bar_tb);   // (6) T Diag(b), Aqk, Kb^T of chunk cc for the consumer
+            warp_arrive(bar_tb);   // (6) T Diag(b), Aqk, Kb^T of chunk cc for the consumer
             if (named_or(1, 128, tmo)) { aborted = true; break; }
         }
     } else {
@@ -1030,7 +1036,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 if (ckd) store_state(ckd, lane_base, v);
             }
             tc_fence_before();
-            barrier_arrive(bar_done);   // (7) chunk c is done: its tiles and parity buffers may be reused
+            warp_arrive(bar_done);   // (7) chunk c is done: its tiles and parity buffers may be reused
         }
         if (!aborted) flush_o();
         if (leader) bulk_wait_all();   // every o tensor store is complete
