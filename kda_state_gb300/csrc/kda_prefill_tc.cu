@@ -336,50 +336,90 @@ __device__ __forceinline__ uint32_t off_sq(int r, int c) {
 // T Diag(beta) into the B tile of U (its upper-right block stays zero from
 // the unit's set-up).  A is the strictly lower part of fp32 [32][AS] (rows
 // scaled by beta; nothing on or above the diagonal is read).  Warp I inverts
-// diagonal block I by column-oriented forward substitution (lane = column,
-// lanes 16-31 idle); warp 0 then forms
-// R = A_10 T_00, and after a two-warp barrier each warp forms one half of
+// the 16 x 16 diagonal block I in two levels: lanes 0-15 invert its two 8 x 8
+// diagonal blocks by column-oriented forward substitution (lane = column),
+// then the whole warp forms the lower-left 8 x 8 block as
+//     T_(1,0) = -T_(1,1) (A_(1,0) T_(0,0))
+// (two columns a lane, through an 8 x 8 scratch in qs).  Warp 0 then forms
+// R = A_10 T_00 of the 16 x 16 blocks, and after a two-warp barrier each warp
+// forms one half of
 //     T_10 = -T_11 R
-// (warp-level m16n8k8 TF32 MMAs).  Returns this warp's largest |T Diag(beta)|
-// (NaN if any entry is NaN) in every lane.
+// (warp-level m16n8k8 TF32 MMAs).  The upper-right 8 x 8 of each diagonal
+// block of T stays zero from the unit's set-up.  Returns this warp's largest
+// |T Diag(beta)| (NaN if any entry is NaN) in every lane.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float solve32(uint8_t *sm, uint8_t *tb, const float *beta, int I, int lane) {
+__device__ __forceinline__ float solve32(uint8_t *sm, uint8_t *tb, const float *beta, float *qs, int I, int lane) {
     const float *As = reinterpret_cast<const float *>(sm + SCR_A);
     float *Ts = reinterpret_cast<float *>(sm + SCR_T);
     float *Rs = reinterpret_cast<float *>(sm + SCR_R);
     float tmax = 0.f;
     if (lane < 16) {
-        const int col = lane;
-        const float *Ab = As + 16 * I * AS + 16 * I;
-        float x[16];
+        const int b = lane >> 3, c = lane & 7, r0 = 16 * I + 8 * b;
+        const float *Ab = As + r0 * AS + r0;
+        float4 lo[8], hi[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
+        for (int r = 1; r < 8; ++r) {
+            lo[r] = *reinterpret_cast<const float4 *>(Ab + r * AS);
+            if (r > 4) hi[r] = *reinterpret_cast<const float4 *>(Ab + r * AS + 4);
+        }
+        float x[8];
 #pragma unroll
-        for (int j0 = 0; j0 < 16; j0 += 4) {
-            float4 a[16];
+        for (int r = 0; r < 8; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int r = j0 + 1; r < 16; ++r) a[r] = *reinterpret_cast<const float4 *>(Ab + r * AS + j0);
+        for (int j = 0; j < 7; ++j) {
 #pragma unroll
-            for (int j = j0; j < j0 + 4 && j < 15; ++j) {
-#pragma unroll
-                for (int r = j + 1; r < 16; ++r) {
-                    const float e = (j & 3) == 0 ? a[r].x : (j & 3) == 1 ? a[r].y : (j & 3) == 2 ? a[r].z : a[r].w;
-                    x[r] = fmaf(-e, x[j], x[r]);
-                }
+            for (int r = j + 1; r < 8; ++r) {
+                const float4 &q4 = j < 4 ? lo[r] : hi[r];
+                const float e = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
+                x[r] = fmaf(-e, x[j], x[r]);
             }
         }
-        const int c = 16 * I + col;
-        const float bc = beta[c];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int rr = 16 * I + r;
-            Ts[rr * TS + col] = x[r];
-            const float tv = x[r] * bc;
-            tmax = maxnan3(tmax, fabsf(tv), 0.f);
-            *reinterpret_cast<float *>(tb + off_sq(rr, c)) = tv;
-        }
+        for (int r = 0; r < 8; ++r) Ts[(r0 + r) * TS + 8 * b + c] = x[r];
     }
     __syncwarp();
+    {
+        // the lower-left 8 x 8 block of diagonal block I: lane = (row rl, columns c0, c0 + 1)
+        const int rl = lane >> 2, c0 = 2 * (lane & 3);
+        const float4 a0 = *reinterpret_cast<const float4 *>(As + (16 * I + 8 + rl) * AS + 16 * I);
+        const float4 a1 = *reinterpret_cast<const float4 *>(As + (16 * I + 8 + rl) * AS + 16 * I + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float2 rv = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float2 t = *reinterpret_cast<const float2 *>(Ts + (16 * I + j) * TS + c0);
+            rv.x = fmaf(av[j], t.x, rv.x);
+            rv.y = fmaf(av[j], t.y, rv.y);
+        }
+        *reinterpret_cast<float2 *>(qs + rl * 8 + c0) = rv;
+        __syncwarp();
+        const float4 u0 = *reinterpret_cast<const float4 *>(Ts + (16 * I + 8 + rl) * TS + 8);
+        const float4 u1 = *reinterpret_cast<const float4 *>(Ts + (16 * I + 8 + rl) * TS + 12);
+        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float2 tv = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float2 r2 = *reinterpret_cast<const float2 *>(qs + j * 8 + c0);
+            tv.x = fmaf(-uv[j], r2.x, tv.x);
+            tv.y = fmaf(-uv[j], r2.y, tv.y);
+        }
+        *reinterpret_cast<float2 *>(Ts + (16 * I + 8 + rl) * TS + c0) = tv;
+    }
+    __syncwarp();
+    {
+        // T Diag(b) of diagonal block I: lane = (row lane / 2, 8 columns)
+        const int rr = 16 * I + (lane >> 1), h8 = 8 * (lane & 1), cc = 16 * I + h8;
+        const float4 t0 = *reinterpret_cast<const float4 *>(Ts + rr * TS + h8);
+        const float4 t1 = *reinterpret_cast<const float4 *>(Ts + rr * TS + h8 + 4);
+        const float4 b0 = *reinterpret_cast<const float4 *>(beta + cc);
+        const float4 b1 = *reinterpret_cast<const float4 *>(beta + cc + 4);
+        const float4 v0 = make_float4(t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w);
+        const float4 v1 = make_float4(t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w);
+        tmax = maxnan3(maxnan3(fabsf(v0.x), fabsf(v0.y), fabsf(v0.z)), maxnan3(fabsf(v0.w), fabsf(v1.x), fabsf(v1.y)),
+                       maxnan3(fabsf(v1.z), fabsf(v1.w), 0.f));
+        *reinterpret_cast<float4 *>(tb + off_sq(rr, cc)) = v0;
+        *reinterpret_cast<float4 *>(tb + off_sq(rr, cc + 4)) = v1;
+    }
     const int g = lane >> 2, t4 = lane & 3;
     if (I == 0) {
         // R = A_10 T_00 (rows 16..31, columns 0..15 of A)
@@ -599,6 +639,8 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
         *reinterpret_cast<float *>(tbz + off_sq(r0 + 8, col)) = 0.f;
     }
     if (tid < 4) reinterpret_cast<uint32_t *>(sm + SM_ZERO)[tid] = 0u;
+    // the upper-right 8 x 8 of each diagonal 16 x 16 block of T stays zero
+    if (tid < 128) reinterpret_cast<float *>(sm + SCR_T)[(16 * (tid >> 6) + ((tid >> 3) & 7)) * TS + 8 + (tid & 7)] = 0.f;
     fence_proxy_async();
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -802,7 +844,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 tc_fence_before();
                 named_sync(1, 128);   // A complete
                 if (warp < 2) {
-                    const float tmx = solve32(sm, sm + OP_TB + pc * 4096, beta_s, warp, lane);
+                    const float tmx = solve32(sm, sm + OP_TB + pc * 4096, beta_s, tot + 64 * warp, warp, lane);   // tot: free here
                     if (lane == 0) tbmax[pc * 2 + warp] = tmx;
                 }
             }
