@@ -656,6 +656,15 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
     const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
     // one arrival for the warp, after every lane's earlier accesses (the warp
     // barrier orders them before lane 0's release)
+    // one lane of the warp waits; the warp barrier then orders the other
+    // lanes' accesses after that wait
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        int ok = 1;
+        if (lane == 0) ok = barrier_wait_for(bar, parity, wait_ns);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        return ok != 0;
+    };
     auto warp_arrive = [&](uint32_t bar) {
         __syncwarp();
         if (lane == 0) barrier_arrive(bar);
@@ -797,9 +806,11 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             const int fb1 = named_or(1, 128, bad);
             if (tid == 0) fbf[pc] = fb1;
             warp_arrive(bar_tiles);   // (3) chunk cc's tiles (and its verdict) for the consumer
-            if (!fb1) {
-                // (4) G1 = [K~; Q~] Kb^T (M = 64); A, Aqk read out; T Diag(b)
-                if (tid == 0) {
+            // (4) G1 = [K~; Q~] Kb^T (M = 64) by thread 0, while warps 1-3 rebuild
+            //     Kb^T from Kb once the consumer has finished chunk cc - 1 (its
+            //     update read the previous Kb^T)
+            if (warp == 0) {
+                if (!fb1 && lane == 0) {
                     tc_fence_after();
                     const uint64_t da = sdesc(sbase + OP_QR, 16, 1024), db = sdesc(sbase + OP_KB, 16, 1024);
 #pragma unroll
@@ -809,8 +820,30 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     mma_commit(bar_g1);
                     if (!barrier_wait_for(bar_g1, n_g & 1u, wait_ns)) tmo = 1;
                 }
+            } else {
+                if (cc > 0 && !warp_wait(bar_done, (uint32_t)((cc - 1) & 1))) tmo = 1;
+                // 4 x 4 blocks (tokens 4 l8.., channels 4 kq..), eight lanes of a
+                // phase on one diagonal: the loads and the stores each meet
+                // eight different 16-byte bank groups
+                for (int bk = tid - 32; bk < 256; bk += 96) {
+                    const int l8 = bk & 7, kq = ((bk >> 3) + l8) & 31;
+                    float4 kr[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        kr[i] = *reinterpret_cast<const float4 *>(sm + OP_KB + off32(4 * l8 + i, 4 * kq, 32));
+                    uint8_t *dst = sm + OP_KBT + 4 * kq * 128;
+                    const int sw = 4 * (kq & 1);
+                    *reinterpret_cast<float4 *>(dst + 0 * 128 + ((l8 ^ (sw + 0)) << 4)) = make_float4(kr[0].x, kr[1].x, kr[2].x, kr[3].x);
+                    *reinterpret_cast<float4 *>(dst + 1 * 128 + ((l8 ^ (sw + 1)) << 4)) = make_float4(kr[0].y, kr[1].y, kr[2].y, kr[3].y);
+                    *reinterpret_cast<float4 *>(dst + 2 * 128 + ((l8 ^ (sw + 2)) << 4)) = make_float4(kr[0].z, kr[1].z, kr[2].z, kr[3].z);
+                    *reinterpret_cast<float4 *>(dst + 3 * 128 + ((l8 ^ (sw + 3)) << 4)) = make_float4(kr[0].w, kr[1].w, kr[2].w, kr[3].w);
+                }
+                fence_proxy_async();   // Kb^T is read by the tensor cores
+            }
+            named_sync(1, 128);   // G1 done; Kb^T rebuilt
+            if (!fb1) {
+                // (5) A, Aqk read out; T Diag(b)
                 ++n_g;
-                named_sync(1, 128);
                 tc_fence_after();
                 uint32_t r[32];
                 KDA_TMEM_LD32(lane_base + TM_G, r);   // M = 64: row r in lane 32 (r / 16) + r % 16
@@ -846,30 +879,6 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 if (warp < 2) {
                     const float tmx = solve32(sm, sm + OP_TB + pc * 4096, beta_s, tot + 64 * warp, warp, lane);   // tot: free here
                     if (lane == 0) tbmax[pc * 2 + warp] = tmx;
-                }
-            }
-            // (5) Kb^T, once the consumer has finished chunk cc - 1 (its update
-            //     read the previous Kb^T); rebuilt from Kb
-            if (tid == 0 && cc > 0 && !barrier_wait_for(bar_done, (uint32_t)((cc - 1) & 1), wait_ns)) tmo = 1;
-            named_sync(1, 128);
-            {
-                // 4 x 4 blocks (tokens 4 l8.., channels 4 kq..), eight lanes of a
-                // phase on one diagonal: the loads and the stores each meet
-                // eight different 16-byte bank groups
-                const int l8 = tid & 7, q = tid >> 3;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int kq = (q + 16 * hf + l8) & 31;
-                    float4 kr[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        kr[i] = *reinterpret_cast<const float4 *>(sm + OP_KB + off32(4 * l8 + i, 4 * kq, 32));
-                    uint8_t *dst = sm + OP_KBT + 4 * kq * 128;
-                    const int sw = 4 * (kq & 1);
-                    *reinterpret_cast<float4 *>(dst + 0 * 128 + ((l8 ^ (sw + 0)) << 4)) = make_float4(kr[0].x, kr[1].x, kr[2].x, kr[3].x);
-                    *reinterpret_cast<float4 *>(dst + 1 * 128 + ((l8 ^ (sw + 1)) << 4)) = make_float4(kr[0].y, kr[1].y, kr[2].y, kr[3].y);
-                    *reinterpret_cast<float4 *>(dst + 2 * 128 + ((l8 ^ (sw + 2)) << 4)) = make_float4(kr[0].z, kr[1].z, kr[2].z, kr[3].z);
-                    *reinterpret_cast<float4 *>(dst + 3 * 128 + ((l8 ^ (sw + 3)) << 4)) = make_float4(kr[0].w, kr[1].w, kr[2].w, kr[3].w);
                 }
             }
             fence_proxy_async();
