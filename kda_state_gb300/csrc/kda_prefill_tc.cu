@@ -16,7 +16,7 @@
 // S the state entering it, and (row r scaled per channel)
 //     K~ = K . exp(G),  Q~ = Q . exp(G),  Kb = K . exp(-G):
 //     A   = tril_-1(Diag(b) K~ Kb^T),   Aqk = tril(Q~ Kb^T),   T = (I + A)^-1
-//     P   = [K~; Q~] S                  (K~ S and Q~ S in one product)
+//     P   = [Q~; K~] S                  (Q~ S and K~ S in one product)
 //     U   = T Diag(b) (V - K~ S)
 //     O   = Q~ S + Aqk U
 //     S_L = Diag(exp(G_L)) (S + Kb^T U)
@@ -25,11 +25,13 @@
 // chunk start) serves the whole chunk while its decay stays within 60 nats.
 //
 // Per chunk (every product kind::tf32, fp32 accumulators in TMEM):
-//   G1  [K~; Q~] (64 x 128, smem) x Kb^T                 -> TMEM, M = 64: A, Aqk
-//   P   S^T (TMEM, A operand) x [K~; Q~]^T (smem)        -> TMEM cols 128..191
+//   G1  [Q~; K~] (64 x 128, smem) x Kb^T                 -> TMEM, M = 64: Aqk, A
+//   P   S^T (TMEM, A operand) x [Q~; K~]^T (smem)        -> TMEM cols 128..191
 //   U   V'^T (TMEM) x (T Diag(b))^T (smem)               -> TMEM cols 224..255
-//   O   U^T (TMEM) x Aqk^T, added onto Q~ S               -> TMEM cols 160..191
-//   X   U^T (TMEM) x Kb (smem, as Kb^T rows), added onto S^T -> TMEM cols 0..127
+//   X|O U^T (TMEM) x [Kb^T; Aqk]^T (smem, 160 rows), added onto
+//       [S^T | Q~ S]                                     -> TMEM cols 0..159
+// (an MMA of N up to 128 costs the same as one of N = 32, and so does N =
+// 160: O rides on the state update)
 // and at the end of the chunk one pass over TMEM writes O out and scales X by
 // exp(G_L) into the next chunk's state.  The CUDA cores do the cumulative
 // decays and exponentials (prep), the 32 x 32 unit-lower-triangular inverse
@@ -76,19 +78,21 @@ constexpr int AS = 36;     // row stride (floats) of the fp32 A scratch
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  fp32 operand
 // tiles are K-major with the 128-byte swizzle, 32 channels (128 B) per box.
-// The producer warps (0-3) write [K~; Q~], Kb, Kb^T, A, Aqk, T Diag(b) and the
+// The producer warps (0-3) write [Q~; K~], Kb, Kb^T, A, Aqk, T Diag(b) and the
 // decay factors; the consumer warps (4-7) own v, the state and the recurrent
-// path's scratch.  Tiles read across the two groups one chunk apart are kept
-// by chunk parity.
-constexpr uint32_t OP_QR = 0;          // [K~; Q~]: 64 rows x 128 ch, 4 boxes of 8 KB
+// path's scratch.  T Diag(b) and the decay factors, read across the two
+// groups one chunk apart, are kept by chunk parity; Aqk and Kb^T are single,
+// rewritten only after the consumer has finished the chunk before.
+constexpr uint32_t OP_QR = 0;          // [Q~; K~]: 64 rows x 128 ch, 4 boxes of 8 KB
 constexpr uint32_t RAW_Q = 0;          // raw bf16 tiles (TMA, 32 tokens x 128 ch, two
 constexpr uint32_t RAW_K = 8192;       //  64-channel boxes of 4 KB) of the next chunk,
-constexpr uint32_t RAW_G = 16384;      //  landing over [K~; Q~] once G1 and P have read it
+constexpr uint32_t RAW_G = 16384;      //  landing over [Q~; K~] once G1 and P have read it
 constexpr uint32_t OP_KB = 32768;      // Kb: 32 rows x 128 ch, 4 boxes of 4 KB (B of G1)
 constexpr uint32_t OP_KBT = 49152;     // Kb^T: 128 rows (k) x 32 tokens, one box (B of the update)
-constexpr uint32_t RAW_V = 65536;      // raw bf16 v (TMA), 2 boxes of 4 KB
+constexpr uint32_t OP_AQ = 65536;      // Aqk: 32 rows (r) x 32 tokens, right after Kb^T: rows 128..159 of the
+                                       // update's B operand [Kb^T; Aqk] (N = 160: X^T and O^T in one product)
 constexpr uint32_t OP_TB = 73728;      // T Diag(b) by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of U)
-constexpr uint32_t OP_AQ = 81920;      // Aqk by chunk parity: 2 x (32 rows (r) x 32 tokens) (B of O)
+constexpr uint32_t RAW_V = 81920;      // raw bf16 v (TMA), 2 boxes of 4 KB
 constexpr uint32_t OP_OST = 90112;     // o of a full chunk (bf16, 2 boxes of 64 ch x 32 tokens, SW128) for its tensor store
 constexpr uint32_t SCR_A = 98304;      // fp32 Diag(b) K~ Kb^T [32][AS]; A is its strictly lower part
 constexpr uint32_t SCR_T = SCR_A + 32 * AS * 4;   // fp32 T of the diagonal blocks [32][TS]
@@ -109,13 +113,16 @@ static_assert(SCR_A % 16 == 0 && SCR_T % 16 == 0 && SCR_R % 16 == 0 && FB_IN % 1
 static_assert(OP_OST % 1024 == 0, "the o staging tile must be 1024-aligned for its 128-byte swizzle");
 static_assert(SM_ELR % 16 == 0 && SM_TOT % 16 == 0, "factor arrays misaligned");
 static_assert(RAW_G + 8192 <= OP_KB, "raw tiles overflow the Gram operand tile");
-static_assert(OP_TB % 1024 == 0 && OP_AQ % 1024 == 0 && OP_KBT % 1024 == 0, "operand tiles misaligned");
+static_assert(OP_TB % 1024 == 0 && OP_AQ % 1024 == 0 && OP_KBT % 1024 == 0 && RAW_V % 1024 == 0, "operand tiles misaligned");
+static_assert(OP_AQ == OP_KBT + 128 * 128, "Aqk must follow Kb^T: one B operand of 160 rows");
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
 
 // TMEM columns (256 per CTA, two CTAs per SM)
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t TM_X = 0;     // the state, transposed: lane v, column k
-constexpr uint32_t TM_P = 128;   // P^T: columns 128..159 K~ S -> V'^T; 160..191 Q~ S -> O^T
+constexpr uint32_t TM_P = 128;   // P^T: columns 128..159 Q~ S -> O^T (right after X^T); 160..191 K~ S -> V'^T
+constexpr uint32_t TM_O = TM_P;       // O^T
+constexpr uint32_t TM_V = TM_P + 32;  // V'^T
 constexpr uint32_t TM_G = 192;   // the Gram product (M = 64 layout), 32 columns
 constexpr uint32_t TM_U = 224;   // U^T, 32 columns
 
@@ -564,11 +571,11 @@ __device__ __forceinline__ void vprime_half(const uint8_t *vrow, int cv, uint32_
 // the kernel
 //
 // Producer warps 0-3, per chunk j: wait for the raw tiles; prep (cumulative
-// decays, exponentials, [K~; Q~], Kb, exp(G_L)); signal "tiles"; G1; A and Aqk
+// decays, exponentials, [Q~; K~], Kb, exp(G_L)); signal "tiles"; G1; A and Aqk
 // read out; T Diag(b) (warps 0 and 1); once the consumer is done with chunk
 // j - 1, Kb^T; signal "solve".
 // Consumer warps 4-7, per chunk j: wait for "tiles"; P; once P and G1 have
-// read [K~; Q~], request the next raw tiles; V'; wait for "solve"; U, then O
+// read [Q~; K~], request the next raw tiles; V'; wait for "solve"; U, then O
 // and the state update; O out and the state scaled by exp(G_L); signal "done".
 // The producer thus prepares chunk j + 1 while the consumer runs chunk j.
 // ---------------------------------------------------------------------------
@@ -673,7 +680,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
     constexpr uint32_t ID_G1 = idesc_tf32(64, 32);
     constexpr uint32_t ID_P = idesc_tf32(128, 64);
     constexpr uint32_t ID_N32 = idesc_tf32(128, 32);
-    constexpr uint32_t ID_S = idesc_tf32(128, 128);
+    constexpr uint32_t ID_XO = idesc_tf32(128, 160);
     bool aborted = false;
 
     if (warp < 4) {
@@ -792,8 +799,8 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     const float2 kt01 = __fmul2_rn(k01, ef[0]), kt23 = __fmul2_rn(k23, ef[1]);
                     const float2 qt01 = __fmul2_rn(q01, ef[0]), qt23 = __fmul2_rn(q23, ef[1]);
                     const float2 kb01 = __fmul2_rn(k01, eb[0]), kb23 = __fmul2_rn(k23, eb[1]);
-                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(r, k0, 64)) = make_float4(kt01.x, kt01.y, kt23.x, kt23.y);
-                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(32 + r, k0, 64)) =
+                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(32 + r, k0, 64)) = make_float4(kt01.x, kt01.y, kt23.x, kt23.y);
+                    *reinterpret_cast<float4 *>(sm + OP_QR + off32(r, k0, 64)) =
                         make_float4(qt01.x, qt01.y, qt23.x, qt23.y);
                     *reinterpret_cast<float4 *>(sm + OP_KB + off32(r, k0, 32)) = tf32r4(kb01.x, kb01.y, kb23.x, kb23.y);
                 }
@@ -806,7 +813,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             const int fb1 = named_or(1, 128, bad);
             if (tid == 0) fbf[pc] = fb1;
             warp_arrive(bar_tiles);   // (3) chunk cc's tiles (and its verdict) for the consumer
-            // (4) G1 = [K~; Q~] Kb^T (M = 64) by thread 0, while warps 1-3 rebuild
+            // (4) G1 = [Q~; K~] Kb^T (M = 64) by thread 0, while warps 1-3 rebuild
             //     Kb^T from Kb once the consumer has finished chunk cc - 1 (its
             //     update read the previous Kb^T)
             if (warp == 0) {
@@ -849,7 +856,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 KDA_TMEM_LD32(lane_base + TM_G, r);   // M = 64: row r in lane 32 (r / 16) + r % 16
                 if (lane < 16) {
                     const int row = 16 * (lq & 1) + lane;
-                    if (lq < 2) {
+                    if (lq >= 2) {
                         // the whole row, scaled by beta: the inverse reads only
                         // the strictly lower part
                         const float b = beta_s[row];
@@ -868,7 +875,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                             float a4[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) a4[e] = (4 * j + e <= row) ? __uint_as_float(r[4 * j + e]) : 0.f;
-                            *reinterpret_cast<float4 *>(sm + OP_AQ + pc * 4096 + off_sq(row, 4 * j)) =
+                            *reinterpret_cast<float4 *>(sm + OP_AQ + off_sq(row, 4 * j)) =
                                 tf32r4(a4[0], a4[1], a4[2], a4[3]);
                         }
                     }
@@ -948,8 +955,8 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             if (!fb1) {
                 const uint32_t ppar = n_p & 1u;
                 ++n_p;
-                // (2) P^T = S^T [K~; Q~]^T (A from TMEM); once P and G1 have read
-                //     [K~; Q~], the next raw tiles are requested over it
+                // (2) P^T = S^T [Q~; K~]^T (A from TMEM); once P and G1 have read
+                //     [Q~; K~], the next raw tiles are requested over it
                 if (leader) {
                     tc_fence_after();
                     const uint64_t da = sdesc(sbase + OP_QR, 16, 1024);
@@ -977,10 +984,10 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     // rows past the sequence (a partial chunk only) are zero
                     if (L == C) {
 #pragma unroll 1
-                        for (int hf = 0; hf < 2; ++hf) vprime_half<false>(sm + vb + 16 * hf * 128, cv, lane_base + TM_P + 16 * hf, 16, vm);
+                        for (int hf = 0; hf < 2; ++hf) vprime_half<false>(sm + vb + 16 * hf * 128, cv, lane_base + TM_V + 16 * hf, 16, vm);
                     } else {
 #pragma unroll 1
-                        for (int hf = 0; hf < 2; ++hf) vprime_half<true>(sm + vb + 16 * hf * 128, cv, lane_base + TM_P + 16 * hf, L - 16 * hf, vm);
+                        for (int hf = 0; hf < 2; ++hf) vprime_half<true>(sm + vb + 16 * hf * 128, cv, lane_base + TM_V + 16 * hf, L - 16 * hf, vm);
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) vm = maxnan3(vm, __shfl_xor_sync(0xffffffffu, vm, off), 0.f);
@@ -1002,18 +1009,15 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                         const uint64_t dtb = sdesc(sbase + OP_TB + par * 4096, 16, 1024);
 #pragma unroll
                         for (int s = 0; s < 4; ++s)
-                            mma_ts(tmem + TM_U, tmem + TM_P + 8 * s, dtb + (uint64_t)(2 * s), ID_N32, s > 0);
+                            mma_ts(tmem + TM_U, tmem + TM_V + 8 * s, dtb + (uint64_t)(2 * s), ID_N32, s > 0);
                         mma_commit(bar_u);
                         if (c + 1 < nchunks) load_v(t0 + C);
-                        const uint64_t daq = sdesc(sbase + OP_AQ + par * 4096, 16, 1024);
-                        const uint64_t dkt = sdesc(sbase + OP_KBT, 16, 1024);
+                        const uint64_t dkt = sdesc(sbase + OP_KBT, 16, 1024);   // [Kb^T; Aqk]: 160 rows
                         if (barrier_wait_for(bar_u, upar, wait_ns)) {
                             tc_fence_after();
 #pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                mma_ts(tmem + TM_P + 32, tmem + TM_U + 8 * s, daq + (uint64_t)(2 * s), ID_N32, 1);
-                                mma_ts(tmem + TM_X, tmem + TM_U + 8 * s, dkt + (uint64_t)(2 * s), ID_S, 1);
-                            }
+                            for (int s = 0; s < 4; ++s)   // [X^T | O^T] += U^T [Kb^T; Aqk]^T
+                                mma_ts(tmem + TM_X, tmem + TM_U + 8 * s, dkt + (uint64_t)(2 * s), ID_XO, 1);
                             mma_commit(bar_ou);
                             if (!barrier_wait_for(bar_ou, upar, wait_ns)) tmo = 1;
                         } else {
@@ -1040,7 +1044,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t r[16];
-                    KDA_TMEM_LD16(lane_base + TM_P + 32 + 16 * hf, r);
+                    KDA_TMEM_LD16(lane_base + TM_O + 16 * hf, r);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float2 os = __fmul2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
@@ -1076,7 +1080,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             } else {
                 // ---- the chunk by the recurrence, from the state in TMEM ----
                 if (leader) {
-                    if (fb1 && c + 1 < nchunks) load_qkg(t0 + C);   // [K~; Q~] is not read by an MMA
+                    if (fb1 && c + 1 < nchunks) load_qkg(t0 + C);   // [Q~; K~] is not read by an MMA
                     if (fb1 && !barrier_wait_for(bar_v, par, wait_ns)) tmo = 1;
                     if (c + 1 < nchunks) load_v(t0 + C);
                 }
