@@ -615,6 +615,10 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
         return;
     }
     const int nchunks = (eos - bos + C - 1) / C;
+    // the entering state (64 KB) into L2 now: the consumer reads it into TMEM
+    // after the set-up, in four dependent rounds
+    if (si >= 0 && tid >= 128 && tid < 132)
+        prefetch_l2(p.pool + ((size_t)si * p.H + h) * STATE_ELEMS + (tid - 128) * (STATE_ELEMS / 4), STATE_ELEMS);
 
     // ---- set-up -----------------------------------------------------------
     auto load_qkg = [&](int tok) {
