@@ -726,6 +726,7 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             //     reads the zero row.  Every raw value is read before the barrier
             //     after which the operand tiles are written over them.
             float gv[2][4][4];
+            float glo[2][4];   // the octet's row-group-0 sums, folded into the offsets by row group 1
             uint2 wq[2][4], wk[2][4];
             // checks on the raw bf16 bits, two at a time: the largest |k| as an
             // unsigned magnitude (a NaN is above every finite value), the largest
@@ -733,14 +734,14 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
             // with the sign clear; other NaNs reach the decay check through G)
             unsigned kbits = 0u;
             int gbits = (int)0x80008000u;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            // rows past the sequence (a partial chunk only) read the zero row
+            auto load_rows = [&](int hf, bool full) {
                 const int k0 = 4 * cg + 64 * hf;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int r = 8 * o8 + 4 * rg + i;
                     const uint32_t ro = raw_off(r, k0, C);
-                    const bool valid = r < L;
+                    const bool valid = full || r < L;
                     wq[hf][i] = *reinterpret_cast<const uint2 *>(sm + (valid ? RAW_Q + ro : SM_ZERO));
                     wk[hf][i] = *reinterpret_cast<const uint2 *>(sm + (valid ? RAW_K + ro : SM_ZERO));
                     const uint2 wg = *reinterpret_cast<const uint2 *>(sm + (valid ? RAW_G + ro : SM_ZERO));
@@ -749,21 +750,26 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                     gbits = __vmaxs2(gbits, __vmaxs2((int)wg.x, (int)wg.y));
                     kbits = __vmaxu2(kbits, __vmaxu2(wk[hf][i].x & 0x7FFF7FFFu, wk[hf][i].y & 0x7FFF7FFFu));
                 }
-                // inclusive prefix over the thread's 4 rows, then over the two
-                // row groups of the octet (lanes l and l ^ 16)
+            };
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int k0 = 4 * cg + 64 * hf;
+                if (L == C) load_rows(hf, true);
+                else load_rows(hf, false);
+                // inclusive prefix over the thread's 4 rows; row group 1 of the
+                // octet (lanes 16-31) adds row group 0's sums (lanes l ^ 16)
+                // through its offsets
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int i = 1; i < 4; ++i) gv[hf][i][j] += gv[hf][i - 1][j];
                     const float lo = __shfl_xor_sync(0xffffffffu, gv[hf][3][j], 16);
-                    if (rg) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) gv[hf][i][j] += lo;
-                    }
+                    glo[hf][j] = rg ? lo : 0.f;
                 }
                 if (rg)
                     *reinterpret_cast<float4 *>(tot + o8 * 128 + k0) =
-                        make_float4(gv[hf][3][0], gv[hf][3][1], gv[hf][3][2], gv[hf][3][3]);
+                        make_float4(gv[hf][3][0] + glo[hf][0], gv[hf][3][1] + glo[hf][1], gv[hf][3][2] + glo[hf][2],
+                                    gv[hf][3][3] + glo[hf][3]);
             }
             named_sync(1, 128);   // octet sums visible; every raw tile read
             float dmax = 0.f;   // largest decay over the chunk, log2 units (G is non-increasing)
@@ -776,12 +782,12 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 const float4 T3 = *reinterpret_cast<const float4 *>(tot + 384 + k0);
                 const float t0a[4] = {T0.x, T0.y, T0.z, T0.w}, t1a[4] = {T1.x, T1.y, T1.z, T1.w};
                 const float t2a[4] = {T2.x, T2.y, T2.z, T2.w}, t3a[4] = {T3.x, T3.y, T3.z, T3.w};
-                float cj[4];   // G_r log2(e) = G'_r log2(e) + cj, G'_r the octet-local prefix
+                float cj[4];   // G_r log2(e) = G'_r log2(e) + cj, G'_r the thread-local prefix
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float g01 = t0a[j] + t1a[j], g012 = g01 + t2a[j];
                     const float pre = o8 == 0 ? 0.f : (o8 == 1 ? t0a[j] : (o8 == 2 ? g01 : g012));
-                    cj[j] = pre * LOG2E;
+                    cj[j] = (pre + glo[hf][j]) * LOG2E;
                     const float gl2 = (g012 + t3a[j]) * LOG2E;   // G_L log2(e)
                     dmax = maxnan3(dmax, -gl2, 0.f);
                     if (o8 == 0 && rg == 0) elr[pc * 128 + k0 + j] = ex2(gl2);   // exp(G_L)
