@@ -339,7 +339,7 @@ __device__ __forceinline__ uint32_t off_sq(int r, int c) {
 }
 
 // ---------------------------------------------------------------------------
-// 32 x 32 unit-lower-triangular inverse T = (I + A)^-1 by warps 0 and 1, and
+// 32 x 32 unit-lower-triangular inverse T = (I + A)^-1 by two warps (I = 0, 1), and
 // T Diag(beta) into the B tile of U (its upper-right block stays zero from
 // the unit's set-up).  A is the strictly lower part of fp32 [32][AS] (rows
 // scaled by beta; nothing on or above the diagonal is read).  Warp I inverts
@@ -347,7 +347,7 @@ __device__ __forceinline__ uint32_t off_sq(int r, int c) {
 // diagonal blocks by column-oriented forward substitution (lane = column),
 // then the whole warp forms the lower-left 8 x 8 block as
 //     T_(1,0) = -T_(1,1) (A_(1,0) T_(0,0))
-// (two columns a lane, through an 8 x 8 scratch in qs).  Warp 0 then forms
+// (two columns a lane, through an 8 x 8 scratch in qs).  Warp I = 0 then forms
 // R = A_10 T_00 of the 16 x 16 blocks, and after a two-warp barrier each warp
 // forms one half of
 //     T_10 = -T_11 R
@@ -447,7 +447,7 @@ __device__ __forceinline__ float solve32(uint8_t *sm, uint8_t *tb, const float *
             Rs[(g + 8) * TS + 8 * nt + 2 * t4 + 1] = d[3];
         }
     }
-    named_sync(3, 64);   // R (warp 0) and T_11 (warp 1) complete
+    named_sync(3, 64);   // R (warp I = 0) and T_11 (warp I = 1) complete
     // T_10 = -T_11 R, columns 8 I .. 8 I + 7 by warp I; T Diag(b) of the block
     {
         const int nt = I;
@@ -892,10 +892,12 @@ __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant
                 }
                 fence_proxy_async();   // Aqk is read by the tensor cores
                 tc_fence_before();
-                named_sync(1, 128);   // A complete
-                if (warp < 2) {
-                    const float tmx = solve32(sm, sm + OP_TB + pc * 4096, beta_s, tot + 64 * warp, warp, lane);   // tot: free here
-                    if (lane == 0) tbmax[pc * 2 + warp] = tmx;
+                // warps 2-3 read A out of TMEM and invert I + A at once; warps 0-1
+                // read Aqk out beside them
+                if (warp >= 2) {
+                    named_sync(3, 64);   // A complete
+                    const float tmx = solve32(sm, sm + OP_TB + pc * 4096, beta_s, tot + 64 * (warp - 2), warp - 2, lane);   // tot: free here
+                    if (lane == 0) tbmax[pc * 2 + warp - 2] = tmx;
                 }
             }
             fence_proxy_async();
