@@ -35,8 +35,8 @@
 // and at the end of the chunk one pass over TMEM writes O out and scales X by
 // exp(G_L) into the next chunk's state.  The CUDA cores do the cumulative
 // decays and exponentials (prep), the 32 x 32 unit-lower-triangular inverse
-// (16 x 16 blocks: substitution on the diagonal, warp-level TF32 MMAs off it),
-// V' = V - K~ S in TMEM, and the read-outs.  The next chunk's prep runs while
+// (8 x 8 substitutions and an 8 x 8 product per diagonal 16 x 16 block,
+// warp-level TF32 MMAs off it), V' = V - K~ S in TMEM, and the read-outs.  The next chunk's prep runs while
 // this chunk's U, O and state-update products are on the tensor cores.
 // Kb and Aqk are rounded to TF32 to nearest by the CUDA cores that write them;
 // K~, Q~, V' and T Diag(b) are written unrounded, and they and the TMEM
@@ -571,12 +571,12 @@ __device__ __forceinline__ void vprime_half(const uint8_t *vrow, int cv, uint32_
 // the kernel
 //
 // Producer warps 0-3, per chunk j: wait for the raw tiles; prep (cumulative
-// decays, exponentials, [Q~; K~], Kb, exp(G_L)); signal "tiles"; G1; A and Aqk
-// read out; T Diag(b) (warps 0 and 1); once the consumer is done with chunk
-// j - 1, Kb^T; signal "solve".
+// decays, exponentials, [Q~; K~], Kb, exp(G_L)); signal "tiles"; G1 (thread 0)
+// beside Kb^T (warps 1-3, once the consumer is done with chunk j - 1); A read
+// out and T Diag(b) (warps 2-3) beside Aqk read out (warps 0-1); signal "solve".
 // Consumer warps 4-7, per chunk j: wait for "tiles"; P; once P and G1 have
-// read [Q~; K~], request the next raw tiles; V'; wait for "solve"; U, then O
-// and the state update; O out and the state scaled by exp(G_L); signal "done".
+// read [Q~; K~], request the next raw tiles; V'; wait for "solve"; U, then the
+// state update with O; O out and the state scaled by exp(G_L); signal "done".
 // The producer thus prepares chunk j + 1 while the consumer runs chunk j.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(NT, 2) prefill_tc_kernel(const __grid_constant__ Params p) {
